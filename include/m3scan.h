@@ -1,0 +1,174 @@
+/*
+ * m3scan.h -- C ABI of the Mamba-3 SSM state scan library (libm3scan.so).
+ *
+ * The scan is the hot path of a Mamba-3 mixer layer ("Together AI announces
+ * Mamba-3", architecture sections 1-3): an exponential-trapezoid
+ * (second-order) discretisation, a complex-valued state applied as a
+ * block-diagonal 2x2 rotation (the "RoPE trick"), and SISO or rank-R MIMO
+ * input/output.  Per (sequence, head) unit, with N/2 complex state pairs k
+ * and head dimension P:
+ *
+ *   a_t[k]    = exp(dt_t * (A + i*theta_t[k]))
+ *   u_t[k][p] = sum_r (B_t[r][2k] + i*B_t[r][2k+1]) * x_t[r][p]
+ *   h_t[k][p] = a_t[k]*h_{t-1}[k][p] + (1-lam_t)*dt_t*a_t[k]*u_{t-1}[k][p]
+ *               + lam_t*dt_t*u_t[k][p]
+ *   y_t[r][p] = sum_k Re(conj(C_t[r][2k] + i*C_t[r][2k+1]) * h_t[k][p]) + D*x_t[r][p]
+ *
+ * u_{-1} comes from the state's carry (the previous token's B and x), zero
+ * for a fresh state.  After a call the state holds h of the last token and
+ * the carry holds that token's (B, x), so calls chain exactly: a prefill of
+ * L tokens equals a prefill of L1 tokens followed by L - L1 tokens or by
+ * single-token decode steps.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are device pointers, dense, row-major, last index innermost.
+ *     The caller owns every input and output buffer; the library owns only
+ *     the m3_state objects it allocates.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns before it completes.  Nothing synchronises.
+ *   - Every call returns an m3_status.  No exception crosses the ABI and no
+ *     kernel traps.  A kernel that gives up a bounded wait records
+ *     M3_ERR_TIMEOUT in a device status word that m3_device_status() reads.
+ *   - x, B, C, theta, y and the state must be 16-byte aligned.
+ *   - Floating point: inputs are f32 or bf16 (in_dtype); dt, lam and theta
+ *     share that type; A, D, y and the state are f32; all arithmetic is f32
+ *     (tensor-core products take bf16 operands with f32 accumulation).
+ */
+#ifndef M3SCAN_H
+#define M3SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the shared library (built with hidden default visibility). */
+#if defined(__GNUC__)
+#define M3_API __attribute__((visibility("default")))
+#else
+#define M3_API
+#endif
+
+typedef enum m3_status {
+  M3_OK = 0,
+  M3_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, dims that do not match  */
+  M3_ERR_UNSUPPORTED = 2, /* a valid request this build has no kernel for (shape, dtype)    */
+  M3_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                   */
+  M3_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (read by m3_device_status) */
+  M3_ERR_ALLOC = 5        /* device memory allocation failed                               */
+} m3_status;
+
+typedef enum m3_dtype { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
+
+/* Which prefill kernel runs. */
+typedef enum m3_algo {
+  M3_ALGO_AUTO = 0,      /* chunked tensor-core path when the shape has one, else recurrent */
+  M3_ALGO_RECURRENT = 1, /* token-by-token f32 recurrence on CUDA cores (any shape)          */
+  M3_ALGO_CHUNKED = 2    /* chunked tcgen05/TMEM path (bf16 inputs, supported shapes only)   */
+} m3_algo;
+
+/* Problem sizes. */
+typedef struct m3_dims {
+  int32_t batch;    /* sequences (state slots)                                   */
+  int32_t nheads;   /* H                                                          */
+  int32_t headdim;  /* P (even)                                                   */
+  int32_t dstate;   /* N (even): N/2 complex pairs                                */
+  int32_t rank;     /* R: 1 = SISO, R > 1 = MIMO                                  */
+  int32_t in_dtype; /* m3_dtype of x, B, C, dt, lam, theta and of the carry       */
+} m3_dims;
+
+/* Opaque recurrent state: h, the previous-token carry, and its dims. */
+typedef struct m3_state m3_state;
+
+/* Raw device pointers of a state (for initialisation, inspection, tests). */
+typedef struct m3_state_ptrs {
+  m3_dims dims;
+  float* h;     /* [batch][H][N/2][P][2] f32, (re, im) innermost     */
+  void* prev_B; /* [batch][H][R][N] in_dtype: the last token's B      */
+  void* prev_x; /* [batch][H][R][P] in_dtype: the last token's x      */
+} m3_state_ptrs;
+
+/* Prefill over a whole sequence batch (or a packed variable-length batch). */
+typedef struct m3_prefill_args {
+  m3_dims dims;   /* dims.batch rows; 1 when cu_seqlens is given                      */
+  int64_t seqlen; /* L: tokens per row (total packed tokens with cu_seqlens)           */
+  int32_t chunk;  /* tokens per chunk for M3_ALGO_CHUNKED; 0 = the kernel's default    */
+  int32_t algo;   /* m3_algo                                                            */
+  const void* x;     /* [batch][L][H][R][P]   in_dtype */
+  const void* B;     /* [batch][L][H][R][N]   in_dtype */
+  const void* C;     /* [batch][L][H][R][N]   in_dtype */
+  const void* dt;    /* [batch][L][H]         in_dtype, > 0 */
+  const void* lam;   /* [batch][L][H]         in_dtype, in [0, 1] */
+  const void* theta; /* [batch][L][H][N/2]    in_dtype */
+  const float* A;    /* [H] f32, < 0 */
+  const float* D;    /* [H] f32 */
+  const int32_t* cu_seqlens; /* device [nseq+1], nondecreasing, cu[0] = 0, cu[nseq] = L; or NULL */
+  int32_t nseq;              /* sequences in the packed batch (ignored without cu_seqlens) */
+  float* y;                  /* [batch][L][H][R][P] f32 output */
+} m3_prefill_args;
+
+/* One decode step: a single new token per sequence. */
+typedef struct m3_decode_args {
+  m3_dims dims;
+  const void* x;     /* [batch][H][R][P] in_dtype */
+  const void* B;     /* [batch][H][R][N] in_dtype */
+  const void* C;     /* [batch][H][R][N] in_dtype */
+  const void* dt;    /* [batch][H]       in_dtype */
+  const void* lam;   /* [batch][H]       in_dtype */
+  const void* theta; /* [batch][H][N/2]  in_dtype */
+  const float* A;    /* [H] f32 */
+  const float* D;    /* [H] f32 */
+  float* y;          /* [batch][H][R][P] f32 output */
+} m3_decode_args;
+
+/*
+ * Allocate a state for `dims` and zero it on `stream` (h = 0, no carry).
+ * *out receives the handle.  Errors: M3_ERR_INVALID_ARG (bad dims or null
+ * out), M3_ERR_ALLOC, M3_ERR_CUDA.
+ */
+M3_API m3_status m3_state_alloc(const m3_dims* dims, m3_state** out, void* stream);
+
+/* Free a state (synchronises the device first).  NULL is accepted. */
+M3_API m3_status m3_state_free(m3_state* st);
+
+/* Fill *out with the state's dims and device pointers. */
+M3_API m3_status m3_state_view(const m3_state* st, m3_state_ptrs* out);
+
+/*
+ * Prefill: run the scan over every token of args->x etc. and write y.
+ * With st == NULL every sequence starts from h = 0 without a carry and no
+ * state is kept.  With a state, each sequence starts from its slot's h and
+ * carry and the slot receives the final h and the last token's (B, x);
+ * st's dims must equal args->dims, except that with cu_seqlens st's batch
+ * is nseq.  With cu_seqlens (batch must be 1), each packed sequence
+ * [cu[s], cu[s+1]) is its own unit: h and the carry restart at every
+ * boundary (from the state slot s when st is given).
+ * Errors: M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED (algo CHUNKED on a shape
+ * or dtype without a chunked kernel), M3_ERR_CUDA.
+ */
+M3_API m3_status m3_scan_prefill(const m3_prefill_args* args, m3_state* st, void* stream);
+
+/*
+ * Decode step: advance every sequence of st by one token, write y, and
+ * replace the carry with this token's (B, x).  args->dims must equal st's.
+ * Errors: M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA.
+ */
+M3_API m3_status m3_decode_step(const m3_decode_args* args, m3_state* st, void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the library's device status word.
+ * Returns M3_OK, or M3_ERR_TIMEOUT if a kernel gave up a bounded wait since
+ * the last check, or M3_ERR_CUDA if the synchronisation itself failed.
+ */
+M3_API m3_status m3_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+M3_API const char* m3_status_string(m3_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3SCAN_H */

@@ -1,0 +1,208 @@
+"""Mamba-3 SSM state scan on B300 (sm_103a): Python binding of libm3scan.
+
+The compute runs in the CUDA library ``libm3scan.so`` built from
+``csrc/`` (see ``build.py``); its C ABI is ``include/m3scan.h``.  This
+module only marshals arguments: torch tensors in, raw device pointers and
+sizes out, one ctypes call per entry point, same names as the C ABI.
+There is no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libm3scan.so")
+
+M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_ERR_ALLOC = range(6)
+M3_F32, M3_BF16 = 0, 1
+M3_ALGO_AUTO, M3_ALGO_RECURRENT, M3_ALGO_CHUNKED = 0, 1, 2
+
+SYMBOLS = ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
+           "m3_decode_step", "m3_device_status", "m3_status_string")
+
+
+class M3Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {m3_status_string(status)} (status {status})")
+
+
+class m3_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
+                ("dstate", ctypes.c_int32), ("rank", ctypes.c_int32), ("in_dtype", ctypes.c_int32)]
+
+
+class m3_state_ptrs(ctypes.Structure):
+    _fields_ = [("dims", m3_dims), ("h", ctypes.c_void_p), ("prev_B", ctypes.c_void_p),
+                ("prev_x", ctypes.c_void_p)]
+
+
+class m3_prefill_args(ctypes.Structure):
+    _fields_ = [("dims", m3_dims), ("seqlen", ctypes.c_int64), ("chunk", ctypes.c_int32),
+                ("algo", ctypes.c_int32)] + \
+        [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "cu_seqlens")] + \
+        [("nseq", ctypes.c_int32), ("y", ctypes.c_void_p)]
+
+
+class m3_decode_args(ctypes.Structure):
+    _fields_ = [("dims", m3_dims)] + \
+        [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "y")]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libm3scan.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libm3scan.so is not built ({path}); run state_space_sequence_06_b300/build.py")
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    lib.m3_state_alloc.argtypes = [ctypes.POINTER(m3_dims), ctypes.POINTER(vp), vp]
+    lib.m3_state_free.argtypes = [vp]
+    lib.m3_state_view.argtypes = [vp, ctypes.POINTER(m3_state_ptrs)]
+    lib.m3_scan_prefill.argtypes = [ctypes.POINTER(m3_prefill_args), vp, vp]
+    lib.m3_decode_step.argtypes = [ctypes.POINTER(m3_decode_args), vp, vp]
+    lib.m3_device_status.argtypes = [vp]
+    for f in ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
+              "m3_decode_step", "m3_device_status"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.m3_status_string.argtypes = [ctypes.c_int]
+    lib.m3_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def m3_status_string(status: int) -> str:
+    return load_library().m3_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != M3_OK:
+        raise M3Error(rc, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return M3_BF16
+    if t.dtype == torch.float32:
+        return M3_F32
+    raise ValueError(f"unsupported input dtype {t.dtype}")
+
+
+class _DeviceArray:
+    """Zero-copy view of library-owned device memory (CUDA array interface)."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+class State:
+    """A library-allocated m3_state; ``h``, ``prev_B`` and ``prev_x`` are
+    zero-copy torch views of its device buffers."""
+
+    def __init__(self, handle, dims: m3_dims):
+        self.handle = handle
+        self.dims = dims
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+    def views(self):
+        p = m3_state_view(self)
+        d = p.dims
+        K = d.dstate // 2
+        ts = "<f4" if d.in_dtype == M3_F32 else "<u2"
+        h = torch.as_tensor(_DeviceArray(p.h, (d.batch, d.nheads, K, d.headdim, 2), "<f4"), device="cuda")
+        pB = torch.as_tensor(_DeviceArray(p.prev_B, (d.batch, d.nheads, d.rank, d.dstate), ts), device="cuda")
+        px = torch.as_tensor(_DeviceArray(p.prev_x, (d.batch, d.nheads, d.rank, d.headdim), ts), device="cuda")
+        if d.in_dtype == M3_BF16:
+            pB, px = pB.view(torch.bfloat16), px.view(torch.bfloat16)
+        return h, pB, px
+
+    def free(self):
+        if self.handle:
+            m3_state_free(self)
+            self.handle = None
+
+
+def make_dims(batch, nheads, headdim, dstate, rank, in_dtype) -> m3_dims:
+    return m3_dims(batch, nheads, headdim, dstate, rank, in_dtype)
+
+
+def m3_state_alloc(dims: m3_dims, stream=None) -> State:
+    h = ctypes.c_void_p()
+    _check(load_library().m3_state_alloc(ctypes.byref(dims), ctypes.byref(h), _stream(stream)),
+           "m3_state_alloc")
+    return State(h.value, dims)
+
+
+def m3_state_free(state: State):
+    _check(load_library().m3_state_free(state.handle), "m3_state_free")
+
+
+def m3_state_view(state: State) -> m3_state_ptrs:
+    out = m3_state_ptrs()
+    _check(load_library().m3_state_view(state.handle, ctypes.byref(out)), "m3_state_view")
+    return out
+
+
+def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
+                    cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None):
+    """Prefill.  x [b][L][H][R][P], B/C [b][L][H][R][N], dt/lam [b][L][H],
+    theta [b][L][H][N/2] (all bf16 or all f32), A/D [H] f32, y [b][L][H][R][P]
+    f32 (written).  ``cu_seqlens`` (int32 CUDA tensor) packs sequences in a
+    batch of one row."""
+    b, L, H, R, P = x.shape
+    N = B.shape[-1]
+    a = m3_prefill_args()
+    a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
+    a.seqlen, a.chunk, a.algo = L, chunk, algo
+    a.x, a.B, a.C, a.dt, a.lam, a.theta = (_ptr(t) for t in (x, B, C, dt, lam, theta))
+    a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
+    if cu_seqlens is not None:
+        a.cu_seqlens = _ptr(cu_seqlens)
+        a.nseq = cu_seqlens.numel() - 1
+    _check(load_library().m3_scan_prefill(ctypes.byref(a), state.handle if state else None,
+                                          _stream(stream)), "m3_scan_prefill")
+
+
+def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None):
+    """One decode step.  x [b][H][R][P], B/C [b][H][R][N], dt/lam [b][H],
+    theta [b][H][N/2], A/D [H] f32, y [b][H][R][P] f32 (written)."""
+    b, H, R, P = x.shape
+    N = B.shape[-1]
+    a = m3_decode_args()
+    a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
+    a.x, a.B, a.C, a.dt, a.lam, a.theta = (_ptr(t) for t in (x, B, C, dt, lam, theta))
+    a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
+    _check(load_library().m3_decode_step(ctypes.byref(a), state.handle, _stream(stream)),
+           "m3_decode_step")
+
+
+def m3_device_status(stream=None) -> int:
+    return load_library().m3_device_status(_stream(stream))

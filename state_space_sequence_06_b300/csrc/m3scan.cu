@@ -1,0 +1,272 @@
+// C-ABI implementation of libm3scan: argument checks, state objects and
+// kernel dispatch.  The entry points are declared and documented in
+// include/m3scan.h.
+#include <cuda_runtime.h>
+
+#include <new>
+
+#include "common.cuh"
+#include "chunked.cuh"
+#include "decode.cuh"
+#include "recurrent.cuh"
+
+struct m3_state {
+  m3_dims dims;
+  float* h;
+  void* prev_B;
+  void* prev_x;
+};
+
+namespace {
+
+using m3::ceil_div;
+
+size_t dtype_size(int dt) { return dt == M3_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_ok(const m3_dims* d) {
+  return d && d->batch > 0 && d->nheads > 0 && d->headdim > 0 && d->dstate > 0 && d->rank > 0 &&
+         (d->dstate % 2) == 0 && (d->headdim % 2) == 0 &&
+         (d->in_dtype == M3_F32 || d->in_dtype == M3_BF16) && d->headdim <= 1024 &&
+         d->dstate <= 4096 && d->rank <= 64;
+}
+
+bool same_dims(const m3_dims& a, const m3_dims& b) {
+  return a.batch == b.batch && a.nheads == b.nheads && a.headdim == b.headdim &&
+         a.dstate == b.dstate && a.rank == b.rank && a.in_dtype == b.in_dtype;
+}
+
+m3_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- decode
+
+template <typename T, int ITEMS>
+m3_status decode_rank(const m3::DecodeParams& p, int threads, size_t smem, int units,
+                      cudaStream_t s) {
+  switch (p.R) {
+#define M3_DEC(RR)                                                                           \
+  case RR:                                                                                   \
+    m3::decode_step_kernel<T, ITEMS, RR><<<units, threads, smem, s>>>(p);                    \
+    return launch_status();
+    M3_DEC(1) M3_DEC(4)
+#undef M3_DEC
+    default:
+      if (p.R > 8) return M3_ERR_UNSUPPORTED;
+      m3::decode_step_kernel<T, ITEMS, 0><<<units, threads, smem, s>>>(p);
+      return launch_status();
+  }
+}
+
+template <typename T>
+m3_status decode_launch(m3::DecodeParams p, int units, cudaStream_t s) {
+  p.K = p.N / 2;
+  p.PP = p.P / 2;
+  if (p.PP > 256) return M3_ERR_UNSUPPORTED;
+  int kg = 256 / p.PP;
+  if (kg > p.K) kg = p.K;
+  p.KG = kg;
+  const int threads = p.PP * kg;
+  int items = ceil_div(p.K, kg);
+  const size_t smem = sizeof(float) * (2 * p.K + 3 * p.R * p.N + 2 * p.R * p.P + kg * p.R * p.P);
+  if (smem > 48 * 1024) return M3_ERR_UNSUPPORTED;
+  if (items <= 1) return decode_rank<T, 1>(p, threads, smem, units, s);
+  if (items <= 2) return decode_rank<T, 2>(p, threads, smem, units, s);
+  if (items <= 4) return decode_rank<T, 4>(p, threads, smem, units, s);
+  if (items <= 8) return decode_rank<T, 8>(p, threads, smem, units, s);
+  if (items <= 16) return decode_rank<T, 16>(p, threads, smem, units, s);
+  return M3_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- recurrent prefill
+
+template <typename T, int KPT, int RR>
+m3_status recurrent_go(const m3::RecurrentParams& p, int units, int threads, size_t smem,
+                       cudaStream_t s) {
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(m3::recurrent_prefill_kernel<T, KPT, RR>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return M3_ERR_CUDA;
+  m3::recurrent_prefill_kernel<T, KPT, RR><<<units, threads, smem, s>>>(p);
+  return launch_status();
+}
+
+template <typename T, int KPT>
+m3_status recurrent_rank(const m3::RecurrentParams& p, int R, int units, int threads, size_t smem,
+                         cudaStream_t s) {
+  if (R == 1) return recurrent_go<T, KPT, 1>(p, units, threads, smem, s);
+  if (R <= 8) return recurrent_go<T, KPT, 0>(p, units, threads, smem, s);
+  return M3_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+m3_status recurrent_launch(m3::RecurrentParams p, int R, int units, cudaStream_t s) {
+  p.K = p.N / 2;
+  // pairs per thread: 8, with up to 32 threads per p; larger N uses 16 or 32
+  int kpt = 8;
+  while (ceil_div(p.K, kpt) > 32) kpt *= 2;
+  if (kpt > 32) return M3_ERR_UNSUPPORTED;
+  int ks = 1;
+  while (ks < ceil_div(p.K, kpt)) ks *= 2;
+  p.KS = ks;
+  const int threads = ceil_div(p.P * ks, 32) * 32;
+  if (threads > 1024) return M3_ERR_UNSUPPORTED;
+  const int RN = R * p.N, RP = R * p.P;
+  auto smem_for = [&](int tb) {
+    return sizeof(float) * ((size_t)(tb + 1) * RN + (size_t)tb * RN + (size_t)(tb + 1) * RP +
+                            (size_t)tb * 2 * p.K + 2 * (size_t)tb);
+  };
+  int tb = 32;
+  while (tb > 1 && smem_for(tb) > 96 * 1024) tb /= 2;
+  p.TB = tb;
+  const size_t smem = smem_for(tb);
+  if (smem > 200 * 1024) return M3_ERR_UNSUPPORTED;
+  switch (kpt) {
+    case 8: return recurrent_rank<T, 8>(p, R, units, threads, smem, s);
+    case 16: return recurrent_rank<T, 16>(p, R, units, threads, smem, s);
+    default: return recurrent_rank<T, 32>(p, R, units, threads, smem, s);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* m3_status_string(m3_status s) {
+  switch (s) {
+    case M3_OK: return "ok";
+    case M3_ERR_INVALID_ARG: return "invalid argument";
+    case M3_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case M3_ERR_CUDA: return "CUDA error";
+    case M3_ERR_TIMEOUT: return "device wait timed out";
+    case M3_ERR_ALLOC: return "device allocation failed";
+  }
+  return "unknown status";
+}
+
+m3_status m3_state_alloc(const m3_dims* dims, m3_state** out, void* stream) {
+  if (!out || !dims_ok(dims)) return M3_ERR_INVALID_ARG;
+  *out = nullptr;
+  const size_t units = (size_t)dims->batch * dims->nheads;
+  const size_t hb = units * dims->dstate * dims->headdim * sizeof(float);
+  const size_t bb = units * dims->rank * dims->dstate * dtype_size(dims->in_dtype);
+  const size_t xb = units * dims->rank * dims->headdim * dtype_size(dims->in_dtype);
+  m3_state* st = new (std::nothrow) m3_state();
+  if (!st) return M3_ERR_ALLOC;
+  st->dims = *dims;
+  if (cudaMalloc(&st->h, hb) != cudaSuccess) {
+    delete st;
+    return M3_ERR_ALLOC;
+  }
+  if (cudaMalloc(&st->prev_B, bb) != cudaSuccess || cudaMalloc(&st->prev_x, xb) != cudaSuccess) {
+    cudaFree(st->h);
+    cudaFree(st->prev_B);
+    delete st;
+    return M3_ERR_ALLOC;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(st->h, 0, hb, s) != cudaSuccess ||
+      cudaMemsetAsync(st->prev_B, 0, bb, s) != cudaSuccess ||
+      cudaMemsetAsync(st->prev_x, 0, xb, s) != cudaSuccess) {
+    cudaFree(st->h);
+    cudaFree(st->prev_B);
+    cudaFree(st->prev_x);
+    delete st;
+    return M3_ERR_CUDA;
+  }
+  *out = st;
+  return M3_OK;
+}
+
+m3_status m3_state_free(m3_state* st) {
+  if (!st) return M3_OK;
+  cudaDeviceSynchronize();
+  m3_status rc = M3_OK;
+  if (cudaFree(st->h) != cudaSuccess) rc = M3_ERR_CUDA;
+  if (cudaFree(st->prev_B) != cudaSuccess) rc = M3_ERR_CUDA;
+  if (cudaFree(st->prev_x) != cudaSuccess) rc = M3_ERR_CUDA;
+  delete st;
+  return rc;
+}
+
+m3_status m3_state_view(const m3_state* st, m3_state_ptrs* out) {
+  if (!st || !out) return M3_ERR_INVALID_ARG;
+  out->dims = st->dims;
+  out->h = st->h;
+  out->prev_B = st->prev_B;
+  out->prev_x = st->prev_x;
+  return M3_OK;
+}
+
+m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
+  if (!a || !st || !dims_ok(&a->dims) || !same_dims(a->dims, st->dims)) return M3_ERR_INVALID_ARG;
+  if (!a->x || !a->B || !a->C || !a->dt || !a->lam || !a->theta || !a->A || !a->D || !a->y)
+    return M3_ERR_INVALID_ARG;
+  if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
+      !aligned16(a->y))
+    return M3_ERR_INVALID_ARG;
+  m3::DecodeParams p{};
+  p.x = a->x; p.B = a->B; p.C = a->C; p.dt = a->dt; p.lam = a->lam; p.theta = a->theta;
+  p.A = a->A; p.D = a->D; p.y = a->y;
+  p.h = st->h; p.prev_B = st->prev_B; p.prev_x = st->prev_x;
+  p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
+  const int units = a->dims.batch * a->dims.nheads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return a->dims.in_dtype == M3_BF16 ? decode_launch<__nv_bfloat16>(p, units, s)
+                                     : decode_launch<float>(p, units, s);
+}
+
+m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) {
+  if (!a || !dims_ok(&a->dims) || a->seqlen < 0) return M3_ERR_INVALID_ARG;
+  if (!a->x || !a->B || !a->C || !a->dt || !a->lam || !a->theta || !a->A || !a->D || !a->y)
+    return M3_ERR_INVALID_ARG;
+  if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
+      !aligned16(a->y))
+    return M3_ERR_INVALID_ARG;
+  if (a->algo < M3_ALGO_AUTO || a->algo > M3_ALGO_CHUNKED) return M3_ERR_INVALID_ARG;
+  const bool varlen = a->cu_seqlens != nullptr;
+  if (varlen && (a->dims.batch != 1 || a->nseq <= 0)) return M3_ERR_INVALID_ARG;
+  const int nseq = varlen ? a->nseq : a->dims.batch;
+  if (st) {
+    m3_dims want = a->dims;
+    want.batch = nseq;
+    if (!same_dims(want, st->dims)) return M3_ERR_INVALID_ARG;
+  }
+  if (a->seqlen == 0) return M3_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int units = nseq * a->dims.nheads;
+  const bool bf16 = a->dims.in_dtype == M3_BF16;
+
+  if (a->algo != M3_ALGO_RECURRENT) {
+    m3_status rc = m3::chunked_prefill(a, st ? st->h : nullptr, st ? st->prev_B : nullptr,
+                                       st ? st->prev_x : nullptr, nseq, s);
+    if (rc != M3_ERR_UNSUPPORTED || a->algo == M3_ALGO_CHUNKED) return rc;
+  }
+  m3::RecurrentParams p{};
+  p.x = a->x; p.B = a->B; p.C = a->C; p.dt = a->dt; p.lam = a->lam; p.theta = a->theta;
+  p.A = a->A; p.D = a->D; p.cu_seqlens = a->cu_seqlens; p.y = a->y;
+  p.h = st ? st->h : nullptr;
+  p.prev_B = st ? st->prev_B : nullptr;
+  p.prev_x = st ? st->prev_x : nullptr;
+  p.L = a->seqlen;
+  p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
+  return bf16 ? recurrent_launch<__nv_bfloat16>(p, a->dims.rank, units, s)
+              : recurrent_launch<float>(p, a->dims.rank, units, s);
+}
+
+m3_status m3_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return M3_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, m3::g_status, sizeof(int)) != cudaSuccess) return M3_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(m3::g_status, &zero, sizeof(int)) != cudaSuccess) return M3_ERR_CUDA;
+    return static_cast<m3_status>(v);
+  }
+  return M3_OK;
+}
+
+}  // extern "C"

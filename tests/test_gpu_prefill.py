@@ -1,0 +1,206 @@
+"""GPU parity of m3_scan_prefill against the oracle (element by element),
+for every prefill kernel, at small sizes with ragged chunks, with initial
+states and carries, packed variable-length batches, and at full size on
+sampled units."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import state_space_sequence_06_b300 as m3
+import synth
+from gpu_util import TOL, assert_close, dev, prefill_gpu, state_for, to_np
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = [m3.M3_ALGO_RECURRENT, m3.M3_ALGO_AUTO]
+
+
+def dims_of(wl, batch=None):
+    return (batch or wl.batch, wl.nheads, wl.headdim, wl.dstate, wl.rank,
+            m3.M3_BF16 if wl.dtype == "bf16" else m3.M3_F32)
+
+
+def oracle_kw(wl, L=None):
+    return dict(batch=wl.batch, L=L if L is not None else wl.seqlen, H=wl.nheads, P=wl.headdim,
+                N=wl.dstate, R=wl.rank, dtype=wl.dtype)
+
+
+def test_tiny_f32_config():
+    """The tiny all-f32 workload (batch 1, L 64, 2 heads, P 16, N 16) at 1e-4."""
+    wl = synth.workloads()["tiny_f32"]
+    inp = synth.prefill_inputs(wl)
+    st = state_for(dims_of(wl))
+    y = prefill_gpu(inp, wl, state=st)
+    yo, ho, pBo, pxo, _ = oracle.prefill(inp, **oracle_kw(wl))
+    assert_close(y.cpu().numpy(), yo, TOL["f32"], "tiny y")
+    h, pB, px = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL["f32"], "tiny h_final")
+    assert np.array_equal(to_np(pB).reshape(pBo.shape), pBo)
+    assert np.array_equal(to_np(px).reshape(pxo.shape), pxo)
+    st.free()
+
+
+SMALL = {
+    "siso": dict(batch=2, seqlen=333, nheads=3, headdim=64, dstate=128, rank=1, chunk=64),
+    "mimo4": dict(batch=2, seqlen=201, nheads=3, headdim=64, dstate=64, rank=4, chunk=32),
+    "siso_long_dt": dict(batch=1, seqlen=517, nheads=2, headdim=64, dstate=128, rank=1, chunk=64, dt_shift=-3.0),
+    "odd_shape": dict(batch=2, seqlen=45, nheads=2, headdim=32, dstate=48, rank=2, chunk=64),
+}
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("case", list(SMALL))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_small_with_state(case, dtype, algo):
+    """Ragged lengths, a random initial state and carry; y, h_final and the
+    carry against the oracle."""
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], dtype=dtype, h0_std=0.3, carry=True, **SMALL[case])
+    inp = synth.prefill_inputs(wl)
+    st = state_for(dims_of(wl), inp["h0"], inp["prev_B"], inp["prev_x"])
+    y = prefill_gpu(inp, wl, state=st, algo=algo)
+    yo, ho, pBo, pxo, _ = oracle.prefill(inp, **oracle_kw(wl), h0=inp["h0"], prev_B=inp["prev_B"],
+                                         prev_x=inp["prev_x"])
+    tol = TOL[dtype]
+    assert_close(y.cpu().numpy(), yo, tol, f"{case} y")
+    h, pB, px = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, tol, f"{case} h_final")
+    assert np.array_equal(to_np(pB).reshape(pBo.shape), pBo)
+    assert np.array_equal(to_np(px).reshape(pxo.shape), pxo)
+    st.free()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_stateless_and_split(algo):
+    """No state: zero start.  Split: prefill(L) = prefill(L1) + prefill(L-L1)
+    through the state, on the GPU."""
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=2, seqlen=300, nheads=2)
+    inp = synth.prefill_inputs(wl)
+    y_full = prefill_gpu(inp, wl, algo=algo).cpu().numpy()
+    yo, _, _, _, _ = oracle.prefill(inp, **oracle_kw(wl))
+    assert_close(y_full, yo, TOL["bf16"], "stateless y")
+    st = state_for(dims_of(wl))
+    L1 = 131
+    head = {k: (v[:, :L1] if v.ndim >= 3 else v) for k, v in inp.items()}
+    tail = {k: (np.ascontiguousarray(v[:, L1:]) if v.ndim >= 3 else v) for k, v in inp.items()}
+    ya = prefill_gpu(head, wl, state=st, algo=algo).cpu().numpy()
+    yb = prefill_gpu(tail, wl, state=st, algo=algo).cpu().numpy()
+    assert_close(np.concatenate([ya, yb], 1), yo, TOL["bf16"], "split y")
+    st.free()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_prefill_then_decode(algo):
+    """GPU prefill of L-k tokens then k GPU decode steps equals the oracle's
+    prefill of all L tokens."""
+    wl = synth.scaled(synth.workloads()["mimo4_b8_l4096"], batch=2, seqlen=100, nheads=2)
+    inp = synth.prefill_inputs(wl)
+    L, k = wl.seqlen, 7
+    st = state_for(dims_of(wl))
+    head = {n: (v[:, :L - k] if v.ndim >= 3 else v) for n, v in inp.items()}
+    ya = prefill_gpu(head, wl, state=st, algo=algo).cpu().numpy()
+    b, H, R, P = wl.batch, wl.nheads, wl.rank, wl.headdim
+    y = torch.empty((b, H, R, P), dtype=torch.float32, device="cuda")
+    A, D = dev(inp["A"]), dev(inp["D"])
+    yd = []
+    for t in range(L - k, L):
+        tt = {n: dev(np.ascontiguousarray(inp[n][:, t])) for n in ("x", "B", "C", "dt", "lam", "theta")}
+        m3.m3_decode_step(tt["x"], tt["B"], tt["C"], tt["dt"], tt["lam"], tt["theta"], A, D, y, st)
+        yd.append(y.cpu().numpy())
+    yo, ho, _, _, _ = oracle.prefill(inp, **oracle_kw(wl))
+    got = np.concatenate([ya, np.stack(yd, 1)], 1)
+    assert_close(got, yo, TOL["bf16"], "prefill+decode y")
+    h, _, _ = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL["bf16"], "prefill+decode h")
+    st.free()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_varlen_small(algo):
+    """Packed batch with an empty sequence, a one-token sequence and ragged
+    ones; per-sequence initial states; state and carry restart at each
+    boundary."""
+    lens = [37, 1, 0, 130, 64, 65]
+    cu = synth.varlen_cu_seqlens(lens)
+    wl = synth.scaled(synth.workloads()["varlen_16"], seqlen=int(cu[-1]), nheads=3, nseq=len(lens),
+                      cu_seqlens=cu, h0_std=0.2, carry=True)
+    wl_state = synth.scaled(wl, batch=len(lens))
+    inp = synth.prefill_inputs(wl)
+    init = synth.prefill_inputs(wl_state)  # per-sequence h0 and carry
+    st = state_for(dims_of(wl, batch=len(lens)), init["h0"], init["prev_B"], init["prev_x"])
+    y = prefill_gpu(inp, wl, state=st, cu=cu, algo=algo).cpu().numpy()
+    yo, ho, pBo, pxo, _ = oracle.prefill(inp, **oracle_kw(wl), cu_seqlens=cu, h0=init["h0"],
+                                         prev_B=init["prev_B"], prev_x=init["prev_x"])
+    assert_close(y, yo, TOL["bf16"], "varlen y")
+    h, pB, px = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL["bf16"], "varlen h")
+    assert np.array_equal(to_np(pB).reshape(pBo.shape), pBo)
+    assert np.array_equal(to_np(px).reshape(pxo.shape), pxo)
+    st.free()
+
+
+def test_empty_sequence_is_noop():
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=1, seqlen=0, nheads=1)
+    x = torch.empty((1, 0, 1, 1, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((1, 0, 1, 1, 128), dtype=torch.bfloat16, device="cuda")
+    s = torch.empty((1, 0, 1), dtype=torch.bfloat16, device="cuda")
+    th = torch.empty((1, 0, 1, 64), dtype=torch.bfloat16, device="cuda")
+    A = torch.full((1,), -1.0, device="cuda")
+    y = torch.empty((1, 0, 1, 1, 64), device="cuda")
+    st = state_for(dims_of(wl))
+    h, _, _ = st.views()
+    h.fill_(0.5)
+    # empty tensors have no storage: pass aligned placeholders through the raw ABI
+    buf = torch.empty(64, dtype=torch.float32, device="cuda")
+    a = m3.m3_prefill_args()
+    a.dims = m3.make_dims(1, 1, 64, 128, 1, m3.M3_BF16)
+    a.seqlen = 0
+    for f in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "y"):
+        setattr(a, f, buf.data_ptr())
+    import ctypes
+    assert m3.load_library().m3_scan_prefill(ctypes.byref(a), st.handle, None) == m3.M3_OK
+    torch.cuda.synchronize()
+    assert torch.all(h == 0.5)
+    st.free()
+    del x, B, s, th, A, y
+
+
+def test_invalid_arguments_return_status():
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=2, seqlen=8, nheads=2)
+    inp = synth.prefill_inputs(wl)
+    st = state_for(dims_of(wl, batch=3))  # wrong batch for this call
+    with pytest.raises(m3.M3Error) as e:
+        prefill_gpu(inp, wl, state=st)
+    assert e.value.status == m3.M3_ERR_INVALID_ARG
+    st.free()
+    wl32 = synth.scaled(wl, dtype="f32")
+    with pytest.raises(m3.M3Error) as e:
+        prefill_gpu(synth.prefill_inputs(wl32), wl32, algo=m3.M3_ALGO_CHUNKED)
+    assert e.value.status == m3.M3_ERR_UNSUPPORTED
+
+
+FULL = ["siso_b8_l4096", "mimo4_b8_l4096", "long_l16384", "varlen_16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_units(name):
+    """Full-size workloads in the benchmark's launch configuration; the
+    oracle checks every token of sampled units (first, last, random)."""
+    wl = synth.workloads()[name]
+    inp = synth.prefill_inputs(wl)
+    cu = wl.cu_seqlens if wl.kind == "varlen" else None
+    nseq = wl.nseq if cu is not None else wl.batch
+    st = state_for(dims_of(wl, batch=nseq))
+    y = prefill_gpu(inp, wl, state=st, cu=cu)
+    assert m3.m3_device_status() == m3.M3_OK
+    rng = np.random.default_rng(1)
+    U = nseq * wl.nheads
+    units = sorted(set([0, U - 1] + list(rng.choice(U, 6, replace=False))))
+    yo, ho, _, _, spans = oracle.prefill(inp, **oracle_kw(wl), cu_seqlens=cu, units=units)
+    yg = y.cpu().numpy()
+    h, _, _ = st.views()
+    hg = to_np(h).reshape((U,) + ho.shape[1:])
+    for i, (u, (b, t0, n, hd, _)) in enumerate(zip(units, spans)):
+        assert_close(yg[b, t0:t0 + n, hd], yo[u], TOL[wl.dtype], f"{name} unit {u} y")
+        assert_close(hg[u], ho[i], TOL[wl.dtype], f"{name} unit {u} h")
+    st.free()
