@@ -204,3 +204,41 @@ def test_full_size_sampled_units(name):
         assert_close(yg[b, t0:t0 + n, hd], yo[u], TOL[wl.dtype], f"{name} unit {u} y")
         assert_close(hg[u], ho[i], TOL[wl.dtype], f"{name} unit {u} h")
     st.free()
+
+
+CHUNKED_SHAPES = [(128, 1, 64), (64, 1, 64), (64, 4, 32), (64, 2, 32), (128, 2, 32)]
+
+
+@pytest.mark.parametrize("N,R,Q", CHUNKED_SHAPES)
+@pytest.mark.parametrize("L", [1, 31, 64, 65, 200])
+def test_chunked_shapes_ragged(N, R, Q, L):
+    """Every chunked-kernel variant against the oracle, explicitly selected,
+    at lengths that end inside, at and just past a chunk boundary, with an
+    initial state and a carry."""
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=2, seqlen=L, nheads=3, dstate=N, rank=R,
+                      chunk=Q, h0_std=0.3, carry=True, dt_shift=-3.0)
+    inp = synth.prefill_inputs(wl)
+    st = state_for(dims_of(wl), inp["h0"], inp["prev_B"], inp["prev_x"])
+    y = prefill_gpu(inp, wl, state=st, algo=m3.M3_ALGO_CHUNKED, chunk=Q)
+    assert m3.m3_device_status() == m3.M3_OK
+    yo, ho, pBo, pxo, _ = oracle.prefill(inp, **oracle_kw(wl), h0=inp["h0"], prev_B=inp["prev_B"],
+                                         prev_x=inp["prev_x"])
+    assert_close(y.cpu().numpy(), yo, TOL["bf16"], f"chunked N{N} R{R} Q{Q} L{L} y")
+    h, pB, px = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL["bf16"], f"chunked N{N} R{R} Q{Q} L{L} h")
+    assert np.array_equal(to_np(pB).reshape(pBo.shape), pBo)
+    assert np.array_equal(to_np(px).reshape(pxo.shape), pxo)
+    st.free()
+
+
+def test_chunked_matches_recurrent_closely():
+    """The two GPU kernels agree far inside the tolerance on a mid-size case
+    (the recurrent kernel is f32 throughout)."""
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=2, seqlen=700, nheads=4)
+    inp = synth.prefill_inputs(wl)
+    ya = prefill_gpu(inp, wl, algo=m3.M3_ALGO_CHUNKED).cpu().numpy()
+    yb = prefill_gpu(inp, wl, algo=m3.M3_ALGO_RECURRENT).cpu().numpy()
+    yo, _, _, _, _ = oracle.prefill(inp, **oracle_kw(wl))
+    ea = assert_close(ya, yo, TOL["bf16"], "chunked")
+    eb = assert_close(yb, yo, 1e-5, "recurrent")
+    assert eb < ea
