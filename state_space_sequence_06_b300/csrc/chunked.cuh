@@ -9,28 +9,37 @@
 // cumulative log-decay Lam_i = sum_{s<=i} dt_s A and angle phi_i[k] =
 // sum_{s<=i} dt_s theta_s[k], and psi_i = phi_end - phi_i:
 //
-//   Bt_j = Bhat_j e^{i psi_j},  Ct_t = Chat_t e^{i psi_t}     (rotations, f16)
+//   Bt_j = Bhat_j e^{-i Phi_j},  Ct_t = Chat_t e^{-i Phi_t}   (rotations, f16)
 //   S    = Re(Ct Bt^H)    = realified Ct . Bt^T                (MMA 1)
 //   S'   = S * e^{Lam_t - Lam_j} * w_tj  for j <= t, else 0
 //          w_tt = lam_t dt_t,  w_tj = lam_j dt_j + (1 - lam_{j+1}) dt_{j+1}
 //   Y    = S' X                                                (MMA 2)
-//        + e^{Lam_t} Re(Ct^H R),  R = e^{i phi_end} h'_prev     (MMA 3)
+//        + e^{Lam_t} Re(Ct^H G')                               (MMA 3)
 //        + D x
-//   h'   = e^{Lam_end} R + Bt^T (W X),  W_j = e^{Lam_end - Lam_j} w'_j  (MMA 4)
+//   G'   <- e^{Lam_end} G' + Bt^T (W X),  W_j = e^{Lam_end - Lam_j} w'_j   (MMA 4)
 //
-// where w'_j = lam_j dt_j + (1 - lam_{j+1}) dt_{j+1}, the next token's
-// trapezoid coefficient included (zero past the end of the sequence), so
-// the state carried between chunks already holds the next token's
-// previous-token term.  Every rotation angle is chunk-local (the state
-// absorbs e^{i phi_end} once per chunk) and every decay is the exponential
-// of a difference, so nothing overflows or loses its phase in f32 at any
-// sequence length.
+// Phi_j is the cumulative angle from the start of the sequence, kept
+// reduced modulo 2 pi per pair (the chunk-local sum is added to a running
+// phase once per chunk), so the state G' lives in the rotating frame
+// e^{-i Phi}: the rotation of the state between chunks costs nothing and
+// only the final state is turned back.  w'_j = lam_j dt_j + (1 - lam_{j+1})
+// dt_{j+1} includes the next token's trapezoid coefficient (zero past the
+// end of the sequence), so the state carried between chunks already holds
+// the next token's previous-token term.  Decays are chunk-local and taken
+// as exponentials of differences (or as a product of two factors when the
+// chunk's log-decay range keeps both inside f32), so nothing overflows at
+// any sequence length.
 //
 // One CTA walks the chunks of one (sequence, head) unit and keeps the f32
 // state in TMEM for the whole sequence: the state never travels through
-// HBM between chunks.  Operands are f16 (bf16 inputs convert exactly; f16's
-// 11-bit significand keeps the products within the error budget, bf16's
-// 8 bits do not), accumulation is f32.
+// HBM between chunks.  Operands are f16 with f32 accumulation; bf16 inputs
+// convert exactly.  The rotated B and C, the masked and weighted scores S'
+// and the weighted inputs W X are each carried as a pair hi + lo of f16
+// values (hi = f16(v), lo = f16(v - hi)), and every product takes the
+// hi*hi, hi*lo and lo*hi terms, so those operands keep about 21 bits: one
+// f16 rounding (11 bits) is not enough for outputs 20-40x the rms of y,
+// which the tails of the dt distribution produce.  Only the state copy R
+// that feeds the inter-chunk output stays a single f16.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap and its enums (types only: the driver entry point is looked up at run time)
@@ -57,49 +66,46 @@ struct ChunkParams {
 };
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
-__host__ __device__ constexpr int pow2_at_least(int v) {
-  return v <= 32 ? 32 : v <= 64 ? 64 : v <= 128 ? 128 : v <= 256 ? 256 : 512;
-}
 
 template <int N_, int R_, int Q_>
 struct ChunkCfg {
   static constexpr int N = N_, R = R_, Q = Q_, P = 64;
   static constexpr int K2 = N / 2;  // complex pairs
   static constexpr int MR = Q * R;  // rows of S and Y: (token, rank)
-  static constexpr int NT = 128;    // threads: one warpgroup
   static_assert(MR == 64 || MR == 128, "Q*R must be 64 or 128");
   static_assert(N == 64 || N == 128, "N must be 64 or 128");
-  static_assert(NT % K2 == 0 && Q % (NT / K2) == 0, "angle-scan split");
-  // raw TMA stage: x [Q][R*P], B and C [Q][R*N], theta [Q][K2] (bf16)
-  static constexpr int XR = Q * R * P * 2, BR = Q * R * N * 2, TR = Q * K2 * 2;
-  static constexpr int OFF_XR = 0;
-  static constexpr int OFF_BR = align_up(OFF_XR + XR, 1024);
-  static constexpr int OFF_CR = align_up(OFF_BR + BR, 1024);
-  static constexpr int OFF_TR = align_up(OFF_CR + BR, 1024);
-  static constexpr int STAGE = align_up(OFF_TR + TR, 1024);
-  static constexpr uint32_t STAGE_TX = XR + 2 * BR + TR;
-  // f16 operand tiles, 128B-swizzled, 64-column blocks of [rows x 128 B]
-  static constexpr int CT_BYTES = MR * N * 2;   // Ct, Bt: [MR rows][N], K-major for MMA 1
-  static constexpr int XT_BYTES = MR * P * 2;   // Xt, WXt: [MR rows][P], MN-major B operands
-  static constexpr int ST_BYTES = MR * MR * 2;  // S': [MR rows][MR], K-major A operand
-  static constexpr int RT_BYTES = N * P * 2;    // R: [N rows][P], MN-major B operand
-  static constexpr int OFF_CT = 2 * STAGE;
-  static constexpr int OFF_BT = OFF_CT + CT_BYTES;
-  static constexpr int OFF_XT = OFF_BT + CT_BYTES;
-  static constexpr int OFF_WXT = OFF_XT + XT_BYTES;
-  static constexpr int OFF_ST = OFF_WXT + XT_BYTES;
-  static constexpr int OFF_RT = OFF_ST + ST_BYTES;
+  // warp roles: 8 prologue warps, 4 state/output warps, 1 MMA warp, 1 TMA warp
+  static constexpr int NPRO = 256, NSTA = 128, NT = NPRO + NSTA + 64;
+  static constexpr int W_STA = NPRO / 32, W_MMA = W_STA + NSTA / 32, W_TMA = W_MMA + 1;
+  static_assert(NPRO % K2 == 0 && Q % (NPRO / K2) == 0, "angle-scan split");
+  // one chunk stage: TMA writes bf16 straight into the 128B-swizzled tiles
+  // of C, B (hi parts) and X, which the prologue converts to f16 in place
+  static constexpr int CT_BYTES = MR * N * 2;   // C, B tiles: [N/64 blocks][MR rows][128 B]
+  static constexpr int XT_BYTES = MR * P * 2;   // X, WX tiles: [MR rows][128 B]
+  static constexpr int TH_BYTES = Q * K2 * 2;   // theta [Q][K2] bf16 (unswizzled)
+  static constexpr int OFF_C = 0, OFF_B = CT_BYTES, OFF_CLO = 2 * CT_BYTES, OFF_BLO = 3 * CT_BYTES;
+  static constexpr int OFF_X = 4 * CT_BYTES, OFF_WX = OFF_X + XT_BYTES;
+  static constexpr int OFF_TH = OFF_WX + XT_BYTES;
+  // the lo part of W X reuses the theta area when it is large enough (theta is dead by then)
+  static constexpr bool WXLO_IN_TH = TH_BYTES >= XT_BYTES;
+  static constexpr int OFF_WXLO = WXLO_IN_TH ? OFF_TH : align_up(OFF_TH + TH_BYTES, 1024);
+  static constexpr int STAGE = align_up(WXLO_IN_TH ? OFF_TH + TH_BYTES : OFF_WXLO + XT_BYTES, 1024);
+  static constexpr uint32_t STAGE_TX = 2 * CT_BYTES + XT_BYTES + TH_BYTES;
+  static constexpr int ST_BYTES = MR * MR * 2;  // S' hi and lo: [MR/64 blocks][MR rows][128 B], K-major
+  static constexpr int RT_BYTES = N * P * 2;    // R: [N rows][128 B], MN-major
+  static constexpr int OFF_ST = 2 * STAGE, OFF_STLO = OFF_ST + ST_BYTES, OFF_RT = OFF_STLO + ST_BYTES;
   static constexpr int SMEM = OFF_RT + RT_BYTES + 1024;  // + alignment slack
-  static_assert(SMEM + 4096 <= 232448, "shared memory of one CTA");
-  // TMEM columns (f32): S [MR x MR], Y [MR x P], Yi [MR x P], state [N x P]
-  static constexpr int COL_S = 0, COL_Y = MR, COL_YI = MR + P, COL_G = MR + 2 * P;
-  static constexpr int TMEM_COLS = pow2_at_least(MR + 3 * P);
+  static_assert(SMEM + 6144 <= 232448, "shared memory of one CTA");
+  // TMEM columns (f32): S, Y[2], Yi[2], state
+  static constexpr int COL_S = 0, COL_Y = MR, COL_YI = MR + 2 * P, COL_G = MR + 4 * P;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(COL_G + P <= TMEM_COLS, "TMEM columns");
 };
 
 // TMEM lane holding row `row` of an M-row accumulator (M = 64 uses lanes
 // 0-15 of each 32-lane quarter; M = 128 uses lane = row).
-__device__ __forceinline__ int acc_row_of(int M, int warp, int lane) {
-  return M == 128 ? 32 * warp + lane : (lane < 16 ? 16 * warp + lane : -1);
+__device__ __forceinline__ int acc_row_of(int M, int quarter, int lane) {
+  return M == 128 ? 32 * quarter + lane : (lane < 16 ? 16 * quarter + lane : -1);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -107,30 +113,81 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// v = hi + lo with hi = f16(v) and lo = f16(v - hi), both returned packed as half2.
+__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
+// sin and cos of x after one reduction step by 2*pi (x stays within a few
+// hundred radians here), on the special-function unit.
+__device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
+  const float n = rintf(x * 0.15915494309189535f);
+  __sincosf(fmaf(-n, 6.283185307179586f, x), s, c);
+}
+
 constexpr uint32_t kMaxPolls = 1u << 22;
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms: far beyond any legitimate wait
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait.  Gives up (and makes every role of this CTA give up) when
+// the phase has not completed within kWaitLimitNs, or as soon as another
+// role of this CTA or any other CTA has recorded a failure, so a stalled
+// pipeline ends the launch in well under a second with M3_ERR_TIMEOUT.
+// abort_flag[0] is this CTA's flag, abort_flag[1] the value the device
+// status word held when the CTA started (a failure of an earlier launch
+// must not stop this one).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (umma::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kMaxPolls; ++i) {
+    if (umma::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (abort_flag[0] || *(volatile int*)&g_status != abort_flag[1]) {
+        abort_flag[0] = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  abort_flag[0] = 1;
+  atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
+  return false;
+}
 
 template <int N, int R, int Q>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                            const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_th,
                            const ChunkParams p) {
   using Cfg = ChunkCfg<N, R, Q>;
-  constexpr int P = Cfg::P, K2 = Cfg::K2, MR = Cfg::MR, NT = Cfg::NT;
-  constexpr int G = NT / K2, TPG = Q / G;  // angle scan: G token groups of TPG tokens
+  constexpr int P = Cfg::P, K2 = Cfg::K2, MR = Cfg::MR, NPRO = Cfg::NPRO, NSTA = Cfg::NSTA;
+  constexpr int G = NPRO / K2, TPG = Q / G;  // angle scan: G token groups of TPG tokens
   using namespace umma;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[2];
-  __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2];
+  __shared__ __align__(8) uint64_t bar_sfull, bar_spready, bar_stready, bar_yfull, bar_gfull;
   __shared__ uint32_t tmem_base_s;
-  __shared__ float sDt[Q + 1], sBet[Q + 1], sLam[Q], sGam[Q], sWp[Q], sDw[Q], sELam[Q];
-  __shared__ float sWarpTot[4];
+  __shared__ int s_abort[2];  // this CTA's abort flag; the status word at start
+  // per-chunk scalars, one set per stage
+  __shared__ float sLam[2][Q], sELam[2][Q], sGam[2][Q], sWp[2][Q], sDw[2][Q], sBw[2][Q], sLamEnd[2];
+  // prologue scratch
+  __shared__ float sDt[Q + 1], sBet[Q + 1], sWarpTot[4];
   __shared__ float sPsum[G][K2];
-  __shared__ float2 sEcs[K2];
+  __shared__ float sPhi[K2];  // global angle per pair at the end of the last chunk, in [-pi, pi)
 
   uint8_t* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -147,24 +204,28 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (ntok <= 0) return;  // nothing to do; the state slot keeps its contents
   const int nchunks = (int)((ntok + Q - 1) / Q);
-  const float A = p.A[head], Dh = p.D[head];
+  const float A = p.A[head];
+  volatile int* abort_flag = s_abort;
 
-  uint8_t* Ct = sm + Cfg::OFF_CT;
-  uint8_t* Bt = sm + Cfg::OFF_BT;
-  uint8_t* Xt = sm + Cfg::OFF_XT;
-  uint8_t* WXt = sm + Cfg::OFF_WXT;
   uint8_t* St = sm + Cfg::OFF_ST;
+  uint8_t* Stlo = sm + Cfg::OFF_STLO;
   uint8_t* Rt = sm + Cfg::OFF_RT;
+  auto stage = [&](int s) { return sm + s * Cfg::STAGE; };
 
   if (tid == 0) {
-    mbar_init(saddr(&full_bar[0]), 1);
-    mbar_init(saddr(&full_bar[1]), 1);
-    mbar_init(saddr(&mma_bar), 1);
+    s_abort[0] = 0;
+    s_abort[1] = *(volatile int*)&g_status;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(saddr(&bar_full[s]), 1);
+      mbar_init(saddr(&bar_opready[s]), 1);
+      mbar_init(saddr(&bar_free[s]), 2);  // output epilogue + MMA 4 completion
+    }
+    mbar_init(saddr(&bar_sfull), 1);
+    mbar_init(saddr(&bar_spready), 1);
+    mbar_init(saddr(&bar_stready), 1);
+    mbar_init(saddr(&bar_yfull), 1);
+    mbar_init(saddr(&bar_gfull), 1);
     mbar_init_fence();
-    tma_prefetch_desc(&tm_x);
-    tma_prefetch_desc(&tm_B);
-    tma_prefetch_desc(&tm_C);
-    tma_prefetch_desc(&tm_th);
   }
   if (warp == 0) {
     tmem_alloc(saddr(&tmem_base_s), Cfg::TMEM_COLS);
@@ -174,380 +235,462 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
-  auto issue_tma = [&](int c) {
-    uint8_t* st = sm + (c & 1) * Cfg::STAGE;
-    const uint32_t bar = saddr(&full_bar[c & 1]);
-    const int t = (int)(tok0 + (int64_t)c * Q);
-    mbar_arrive_expect_tx(bar, Cfg::STAGE_TX);
-    tma_load_3d(saddr(st + Cfg::OFF_XR), &tm_x, bar, 0, head, t);
-    tma_load_3d(saddr(st + Cfg::OFF_BR), &tm_B, bar, 0, head, t);
-    tma_load_3d(saddr(st + Cfg::OFF_CR), &tm_C, bar, 0, head, t);
-    tma_load_3d(saddr(st + Cfg::OFF_TR), &tm_th, bar, 0, head, t);
-  };
-  // TMA loads issued into / consumed from each stage (thread 0's count):
-  // use u of stage s completes phase u, so its wait parity is u & 1
-  int issued[2] = {0, 0}, consumed[2] = {0, 0};
-  if (tid == 0) {
-    issue_tma(0);
-    issued[0] = 1;
-    if (nchunks > 1) {
-      issue_tma(1);
-      issued[1] = 1;
-    }
-  }
-
-  // ---- initial state: h'_{-1} = h0 + beta'_0 * sum_r Bprev_r xprev_r^T  (realified rows n)
-  const int g_row = acc_row_of(N, warp, lane);  // state row owned by this thread (-1: none)
-  {
-    const float dt0 = __bfloat162float(p.dt[tok0 * H + head]);
-    const float lm0 = __bfloat162float(p.lam[tok0 * H + head]);
-    const float bet0 = (1.f - lm0) * dt0;
-    for (int cb = 0; cb < P; cb += 16) {
-      float v[16];
+  if (warp < Cfg::W_STA) {
+    // ======================= prologue warps: rotation, operands, S -> S'
+    const int pt = tid;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int k = pt % K2, g = pt / K2;
+    if (pt < K2) sPhi[pt] = 0.f;
+    // dt and lam of token pt of a chunk (token Q: the next chunk's first), loaded one chunk ahead
+    auto load_scalars = [&](int c, float& d, float& l) {
+      d = 0.f;
+      l = 0.f;
+      if (pt <= Q && c < nchunks) {
+        const int64_t i = (int64_t)c * Q + pt;
+        if (i < ntok) {
+          d = __bfloat162float(p.dt[(tok0 + i) * H + head]);
+          l = __bfloat162float(p.lam[(tok0 + i) * H + head]);
+        }
+      }
+    };
+    float d_cur, l_cur;
+    load_scalars(0, d_cur, l_cur);
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      uint8_t* stg = stage(s);
+      float d_nxt, l_nxt;
+      load_scalars(c + 1, d_nxt, l_nxt);
+      if (!group_and(1, NPRO, wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag))) break;
+      // ---- per-token scalars and the inclusive scan of dt * A
+      if (pt <= Q) {
+        sDt[pt] = d_cur;
+        sBet[pt] = (1.f - l_cur) * d_cur;
+        if (pt < Q) sGam[s][pt] = l_cur * d_cur;
+      }
+      // (whole warps take part in the shuffles: tokens Q..QW-1 contribute zero)
+      constexpr int QW = (Q + 31) / 32 * 32;
+      float v = (pt < Q) ? d_cur * A : 0.f;
+      if (pt < QW) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      if (g_row >= 0 && p.h) {
-        const int k = g_row >> 1, ri = g_row & 1;
-        const float* hs = p.h + ((int64_t)unit * K2 + k) * P * 2;
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += u;
+        }
+        if (lane == 31) sWarpTot[warp] = v;
+      }
+      group_sync(1, NPRO);
+      // ---- angle scan, part 1: per-group sums of dt * theta
+      const __nv_bfloat16* th = reinterpret_cast<const __nv_bfloat16*>(stg + Cfg::OFF_TH);
+      {
+        float part = 0.f;
+#pragma unroll 4
+        for (int ii = 0; ii < TPG; ++ii) {
+          const int i = g * TPG + ii;
+          part = fmaf(sDt[i], __bfloat162float(th[i * K2 + k]), part);
+        }
+        sPsum[g][k] = part;
+      }
+      if (pt < Q) {
+        for (int w = 0; w < warp; ++w) v += sWarpTot[w];
+        sLam[s][pt] = v;
+      }
+      group_sync(1, NPRO);
+      const float lam_end = sLam[s][Q - 1];
+      if (pt < Q) {
+        const float wp = sGam[s][pt] + sBet[pt + 1];
+        const float lt = sLam[s][pt];
+        sWp[s][pt] = wp;
+        sDw[s][pt] = __expf(lam_end - lt) * wp;
+        sBw[s][pt] = __expf(-lt) * wp;
+        sELam[s][pt] = __expf(lt);
+        if (pt == 0) sLamEnd[s] = lam_end;
+      }
+      // ---- angle scan, part 2, and the in-place rotation of B and C by
+      //      e^{-i Phi_i}, Phi_i = phase at the chunk start + chunk-local sum
+      {
+        const float phi0 = sPhi[k];
+        float off = 0.f, tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2 + ri];
-        if (p.prev_B) {
+        for (int gg = 0; gg < G; ++gg) {
+          const float sv = sPsum[gg][k];
+          off += (gg < g) ? sv : 0.f;
+          tot += sv;
+        }
+        uint8_t* Bt = stg + Cfg::OFF_B;
+        uint8_t* Ct = stg + Cfg::OFF_C;
+        uint8_t* Blo = stg + Cfg::OFF_BLO;
+        uint8_t* Clo = stg + Cfg::OFF_CLO;
+        const int blk = (2 * k) / 64, col = (2 * k) % 64;
+        float phi = phi0 + off;
+#pragma unroll 2
+        for (int ii = 0; ii < TPG; ++ii) {
+          const int i = g * TPG + ii;
+          phi = fmaf(sDt[i], __bfloat162float(th[i * K2 + k]), phi);
+          float sn, cs;
+          sincos_reduced(-phi, &sn, &cs);
+#pragma unroll
           for (int r = 0; r < R; ++r) {
-            const float b = __bfloat162float(p.prev_B[((int64_t)unit * R + r) * N + g_row]);
-            const __nv_bfloat16* xp = p.prev_x + ((int64_t)unit * R + r) * P + cb;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = fmaf(bet0 * b, __bfloat162float(xp[i]), v[i]);
+            const uint32_t o = blk * (MR * 128) + sw128_offset(i * R + r, col);
+            const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + o));
+            const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
+            uint32_t hi, lo;
+            split_half2(cs * b.x - sn * b.y, sn * b.x + cs * b.y, hi, lo);
+            *reinterpret_cast<uint32_t*>(Bt + o) = hi;
+            *reinterpret_cast<uint32_t*>(Blo + o) = lo;
+            split_half2(cs * cc.x - sn * cc.y, sn * cc.x + cs * cc.y, hi, lo);
+            *reinterpret_cast<uint32_t*>(Ct + o) = hi;
+            *reinterpret_cast<uint32_t*>(Clo + o) = lo;
           }
         }
-      }
-      tmem_st16(tmem + lane_base + Cfg::COL_G + cb, v);
-    }
-    tmem_st_wait();
-  }
-
-  bool ok = true;
-  uint32_t mma_phase = 0;
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int s = c & 1;
-    uint8_t* st = sm + s * Cfg::STAGE;
-    const int64_t ct0 = tok0 + (int64_t)c * Q;  // first token of the chunk
-    const int nvalid = (ntok - (int64_t)c * Q < Q) ? (int)(ntok - (int64_t)c * Q) : Q;
-
-    // ---- per-token scalars: dt, lam (zero past the sequence end), and the next chunk's first token
-    if (tid <= Q) {
-      const bool valid = tid < nvalid || (tid == Q && (int64_t)c * Q + Q < ntok);
-      float d = 0.f, l = 0.f;
-      if (valid) {
-        d = __bfloat162float(p.dt[(ct0 + tid) * H + head]);
-        l = __bfloat162float(p.lam[(ct0 + tid) * H + head]);
-      }
-      sDt[tid] = d;
-      sBet[tid] = (1.f - l) * d;
-      if (tid < Q) sGam[tid] = l * d;
-    }
-    __syncthreads();
-    if (tid < Q) {  // inclusive scan of dt*A over the chunk (whole warps)
-      float v = sDt[tid] * A;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (lane == 31) sWarpTot[warp] = v;
-      sLam[tid] = v;
-    }
-    __syncthreads();
-    if (tid < Q) {
-      float off = 0.f;
-      for (int w = 0; w < warp; ++w) off += sWarpTot[w];
-      sLam[tid] += off;
-    }
-    __syncthreads();
-    const float lam_end = sLam[Q - 1];
-    if (tid < Q) {
-      const float wp = sGam[tid] + sBet[tid + 1];
-      sWp[tid] = wp;
-      sDw[tid] = __expf(lam_end - sLam[tid]) * wp;
-      sELam[tid] = __expf(sLam[tid]);
-    }
-
-    // ---- wait for this chunk's inputs
-    {
-      const bool got = mbar_wait(saddr(&full_bar[s]), (uint32_t)((c >> 1) & 1), kMaxPolls);
-      if (!__syncthreads_and(got)) {
-        ok = false;
-        break;
-      }
-      if (tid == 0) consumed[s] += 1;
-    }
-    const __nv_bfloat16* xr = reinterpret_cast<const __nv_bfloat16*>(st + Cfg::OFF_XR);
-    const uint32_t* Br = reinterpret_cast<const uint32_t*>(st + Cfg::OFF_BR);
-    const uint32_t* Cr = reinterpret_cast<const uint32_t*>(st + Cfg::OFF_CR);
-    const __nv_bfloat16* thr = reinterpret_cast<const __nv_bfloat16*>(st + Cfg::OFF_TR);
-
-    // ---- angle scan and rotation of B and C into the f16 operand tiles
-    {
-      const int k = tid % K2, g = tid / K2;
-      float part = 0.f;
-      for (int ii = 0; ii < TPG; ++ii) {
-        const int i = g * TPG + ii;
-        part = fmaf(sDt[i], __bfloat162float(thr[i * K2 + k]), part);
-      }
-      sPsum[g][k] = part;
-      __syncthreads();
-      float off = 0.f, tot = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        const float v = sPsum[gg][k];
-        off += (gg < g) ? v : 0.f;
-        tot += v;
-      }
-      if (g == 0) {
-        float sn, cs;
-        sincosf(tot, &sn, &cs);
-        sEcs[k] = make_float2(cs, sn);
-      }
-      float phi = off;
-      const int blk = (2 * k) / 64, col = (2 * k) % 64;
-      for (int ii = 0; ii < TPG; ++ii) {
-        const int i = g * TPG + ii;
-        phi = fmaf(sDt[i], __bfloat162float(thr[i * K2 + k]), phi);
-        float sn, cs;
-        sincosf(tot - phi, &sn, &cs);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int row = i * R + r;
-          const float2 b = bf2_to_f2(Br[row * K2 + k]);
-          const float2 cc = bf2_to_f2(Cr[row * K2 + k]);
-          const uint32_t off_b = blk * (MR * 128) + sw128_offset(row, col);
-          *reinterpret_cast<uint32_t*>(Bt + off_b) = pack_half2(cs * b.x - sn * b.y, sn * b.x + cs * b.y);
-          *reinterpret_cast<uint32_t*>(Ct + off_b) = pack_half2(cs * cc.x - sn * cc.y, sn * cc.x + cs * cc.y);
+        group_sync(1, NPRO);  // sDw ready; every thread has read sPhi
+        if (g == 0) {         // advance the running phase by the chunk's angle, reduced to [-pi, pi)
+          const float ph = phi0 + tot;
+          sPhi[k] = fmaf(-rintf(ph * 0.15915494309189535f), 6.283185307179586f, ph);
         }
       }
-    }
-    // ---- X and W X (f16, MN-major [rows j][p])
-    for (int idx = tid; idx < MR * (P / 8); idx += NT) {
-      const int row = idx / (P / 8), c8 = idx % (P / 8);
-      const uint4 raw = *reinterpret_cast<const uint4*>(xr + row * P + c8 * 8);
-      const float w = sDw[row / R];
-      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t hx[4], hw[4];
+      // ---- X to f16 in place, and W X
+      {
+        uint8_t* Xt = stg + Cfg::OFF_X;
+        uint8_t* WXt = stg + Cfg::OFF_WX;
+        uint8_t* WXlo = stg + Cfg::OFF_WXLO;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = bf2_to_f2(rw[q]);
-        hx[q] = pack_half2(f.x, f.y);
-        hw[q] = pack_half2(w * f.x, w * f.y);
+        for (int idx = pt; idx < MR * (P / 8); idx += NPRO) {
+          const int row = idx / (P / 8), c8 = idx % (P / 8);
+          const uint32_t o = sw128_offset(row, c8 * 8);
+          const uint4 raw = *reinterpret_cast<const uint4*>(Xt + o);
+          const float w = sDw[s][row / R];
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hx[4], hw[4], lw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = bf2_to_f2(rw[q]);
+            hx[q] = pack_half2(f.x, f.y);
+            split_half2(w * f.x, w * f.y, hw[q], lw[q]);
+          }
+          *reinterpret_cast<uint4*>(Xt + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
+          *reinterpret_cast<uint4*>(WXt + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
       }
-      const uint32_t o = sw128_offset(row, c8 * 8);
-      *reinterpret_cast<uint4*>(Xt + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
-      *reinterpret_cast<uint4*>(WXt + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    }
-    fence_async_smem();
-    __syncthreads();
-    // the raw stage is consumed: prefetch chunk c + 2 into it
-    if (tid == 0 && c + 2 < nchunks) {
-      issue_tma(c + 2);
-      issued[s] += 1;
-    }
+      fence_async_smem();
+      group_sync(1, NPRO);
+      if (pt == 0) mbar_arrive(saddr(&bar_opready[s]));
+      d_cur = d_nxt;
+      l_cur = l_nxt;
 
-    // ---- MMA 1: S = Ct Bt^T  (M = MR, N = MR, K = N)
-    if (tid == 0) {
+      // ---- S -> S' once MMA 1 is done and MMA 2 of the previous chunk has read S'
+      bool got = wait_or_abort(saddr(&bar_sfull), (uint32_t)(c & 1), abort_flag);
+      if (got && c >= 1) got = wait_or_abort(saddr(&bar_yfull), (uint32_t)((c - 1) & 1), abort_flag);
+      if (!group_and(1, NPRO, got)) break;
       tc_fence_after();
-      constexpr uint32_t idesc = idesc_f16_f32(MR, MR, 0, 0);
+      {
+        const int q4 = warp & 3;
+        const int t = acc_row_of(MR, q4, lane);
+        const int it = t >= 0 ? t / R : 0;
+        // last token held by this warp's rows: column blocks past it are all masked
+        const int it_warp = (MR == 128 ? 32 * q4 + 31 : 16 * q4 + 15) / R;
+        const float elam_t = sELam[s][it], lam_t = sLam[s][it], gam_t = sGam[s][it];
+        const bool factor = lam_end > -60.f;  // e^{Lam_t} and e^{-Lam_j} both stay normal floats
+        constexpr int CPH = MR / 2;           // columns per warp half
+        const int cbeg = (warp >> 2) * CPH;
+        float sv[CPH];
 #pragma unroll
-      for (int ks = 0; ks < N / 16; ++ks) {
-        const uint32_t koff = (ks / 4) * (MR * 128) + (ks % 4) * 32;
-        mma_f16(tmem + Cfg::COL_S, smem_desc(saddr(Ct) + koff, 16, 1024, kSwizzle128B),
-                smem_desc(saddr(Bt) + koff, 16, 1024, kSwizzle128B), idesc, ks > 0);
-      }
-      mma_commit(saddr(&mma_bar));
-    }
-    {
-      const bool got = mbar_wait(saddr(&mma_bar), mma_phase, kMaxPolls);
-      mma_phase ^= 1;
-      if (!__syncthreads_and(got)) {
-        ok = false;
-        break;
-      }
-    }
-    tc_fence_after();
-
-    // ---- S -> S' (causal mask, decay, trapezoid weights), f16, K-major [rows t][cols j]
-    {
-      const int t = acc_row_of(MR, warp, lane);
-      const int it = t >= 0 ? t / R : 0;
-      const float lam_t = sLam[it], gam_t = sGam[it];
-      for (int cb = 0; cb < MR; cb += 16) {
-        float v[16];
-        tmem_ld16(tmem + lane_base + Cfg::COL_S + cb, v);
+        for (int cb = 0; cb < CPH; cb += 16) {
+          float tmp[16];
+          if ((cbeg + cb) / R <= it_warp) tmem_ld16(tmem + lane_base + Cfg::COL_S + cbeg + cb, tmp);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sv[cb + i] = tmp[i];
+        }
         tmem_ld_wait();
         if (t >= 0) {
-          uint32_t hv[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float e[2];
+          for (int cb = 0; cb < CPH; cb += 8) {
+            uint32_t hv[4], lv[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int j = cb + 2 * q + u, jt = j / R;
-              const float w = (jt == it) ? gam_t : sWp[jt];
-              e[u] = (jt <= it) ? v[2 * q + u] * __expf(lam_t - sLam[jt]) * w : 0.f;
+            for (int q = 0; q < 4; ++q) {
+              float e[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int j = cbeg + cb + 2 * q + u, jt = j / R;
+                float val;
+                if (jt < it)
+                  val = factor ? sv[cb + 2 * q + u] * sBw[s][jt] * elam_t
+                               : sv[cb + 2 * q + u] * __expf(lam_t - sLam[s][jt]) * sWp[s][jt];
+                else
+                  val = (jt == it) ? sv[cb + 2 * q + u] * gam_t : 0.f;
+                e[u] = val;
+              }
+              split_half2(e[0], e[1], hv[q], lv[q]);
             }
-            hv[q] = pack_half2(e[0], e[1]);
-          }
-#pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
-            const int j = cb + 8 * hlf;
+            const int j = cbeg + cb;
             const uint32_t o = (j / 64) * (MR * 128) + sw128_offset(t, j % 64);
-            *reinterpret_cast<uint4*>(St + o) = make_uint4(hv[4 * hlf], hv[4 * hlf + 1], hv[4 * hlf + 2], hv[4 * hlf + 3]);
+            *reinterpret_cast<uint4*>(St + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *reinterpret_cast<uint4*>(Stlo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
           }
         }
       }
+      tc_fence_before();
+      fence_async_smem();
+      group_sync(1, NPRO);
+      if (pt == 0) mbar_arrive(saddr(&bar_spready));
     }
-
-    // ---- state step: R = e^{i phi_end} h' (f16 operand), TMEM state <- e^{Lam_end} R
+  } else if (warp < Cfg::W_MMA) {
+    // ======================= state warps: state step and output epilogue
+    const int tt = tid - NPRO;
+    const int q4 = warp & 3;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int g_row = acc_row_of(N, q4, lane);  // state row owned by this thread (-1: none)
+    const float Dh = p.D[head];
+    // initial state: h'_{-1} = h0 + beta'_0 * sum_r Bprev_r xprev_r^T  (realified rows)
     {
-      const float elam_end = __expf(lam_end);
-      const int n = g_row;
-      const float2 ecs = sEcs[n >= 0 ? (n >> 1) : 0];
-      const bool re = (n & 1) == 0;
+      const float dt0 = __bfloat162float(p.dt[tok0 * H + head]);
+      const float lm0 = __bfloat162float(p.lam[tok0 * H + head]);
+      const float bet0 = (1.f - lm0) * dt0;
       for (int cb = 0; cb < P; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, v);
-        tmem_ld_wait();
-        float r[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
-          r[i] = re ? (ecs.x * v[i] - ecs.y * other) : (ecs.y * other + ecs.x * v[i]);
-        }
-        if (n >= 0) {
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if (g_row >= 0 && p.h) {
+          const float* hs = p.h + ((int64_t)unit * K2 + (g_row >> 1)) * P * 2 + (g_row & 1);
 #pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
-            const int pc = cb + 8 * hlf;
-            const uint32_t o = sw128_offset(n, pc);
-            *reinterpret_cast<uint4*>(Rt + o) =
-                make_uint4(pack_half2(r[8 * hlf], r[8 * hlf + 1]), pack_half2(r[8 * hlf + 2], r[8 * hlf + 3]),
-                           pack_half2(r[8 * hlf + 4], r[8 * hlf + 5]), pack_half2(r[8 * hlf + 6], r[8 * hlf + 7]));
+          for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2];
+          if (p.prev_B) {
+            for (int r = 0; r < R; ++r) {
+              const float b = bet0 * __bfloat162float(p.prev_B[((int64_t)unit * R + r) * N + g_row]);
+              const __nv_bfloat16* xp = p.prev_x + ((int64_t)unit * R + r) * P + cb;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = fmaf(b, __bfloat162float(xp[i]), v[i]);
+            }
           }
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] *= elam_end;
-        tmem_st16(tmem + lane_base + Cfg::COL_G + cb, r);
+        tmem_st16(tmem + lane_base + Cfg::COL_G + cb, v);
       }
       tmem_st_wait();
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- MMA 2 (Y = S' X), MMA 3 (Yi = Ct R), MMA 4 (state += Bt^T W X)
-    if (tid == 0) {
+    bool alive = true;
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int s = c & 1;
+      uint8_t* stg = stage(s);
+      const int64_t ct0 = tok0 + (int64_t)c * Q;
+      const int nvalid = (ntok - (int64_t)c * Q < Q) ? (int)(ntok - (int64_t)c * Q) : Q;
+      bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      if (got && c >= 1) got = wait_or_abort(saddr(&bar_gfull), (uint32_t)((c - 1) & 1), abort_flag);
+      if (!group_and(2, NSTA, got)) break;
+      tc_fence_after();
+      // ---- state step (rotating frame): R = G' as the f16 operand of MMA 3, G' <- e^{Lam_end} G'
+      {
+        const float elam_end = __expf(sLamEnd[s]);
+        float v[P];
+#pragma unroll
+        for (int cb = 0; cb < P; cb += 16) {
+          float tmp[16];
+          tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, tmp);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[cb + i] = tmp[i];
+        }
+        tmem_ld_wait();
+        if (g_row >= 0) {
+#pragma unroll
+          for (int pc = 0; pc < P; pc += 8) {
+            const uint32_t o = sw128_offset(g_row, pc);
+            *reinterpret_cast<uint4*>(Rt + o) =
+                make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
+                           pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
+          }
+        }
+#pragma unroll
+        for (int cb = 0; cb < P; cb += 16) {
+          float tmp[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) tmp[i] = v[cb + i] * elam_end;
+          tmem_st16(tmem + lane_base + Cfg::COL_G + cb, tmp);
+        }
+        tmem_st_wait();
+      }
+      fence_async_smem();
+      tc_fence_before();
+      group_sync(2, NSTA);
+      if (tt == 0) mbar_arrive(saddr(&bar_stready));
+      // ---- output: y = Y + e^{Lam_t} Yi + D x
+      if (!group_and(2, NSTA, wait_or_abort(saddr(&bar_yfull), (uint32_t)(c & 1), abort_flag))) break;
       tc_fence_after();
       {
-        constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
+        const uint8_t* Xt = stg + Cfg::OFF_X;
+        const int t = acc_row_of(MR, q4, lane);
+        const int it = t >= 0 ? t / R : 0, rk = t >= 0 ? t % R : 0;
+        const bool valid = t >= 0 && it < nvalid;
+        const float el = sELam[s][it];
+        float* yrow = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
 #pragma unroll
-        for (int ks = 0; ks < MR / 16; ++ks) {
-          const uint32_t aoff = (ks / 4) * (MR * 128) + (ks % 4) * 32;
-          mma_f16(tmem + Cfg::COL_Y, smem_desc(saddr(St) + aoff, 16, 1024, kSwizzle128B),
-                  smem_desc(saddr(Xt) + ks * 2048, MR * 128, 1024, kSwizzle128B), idesc, ks > 0);
-        }
-      }
-      {
-        constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
+        for (int half = 0; half < 2; ++half) {
+          float a[32], b[32];
 #pragma unroll
-        for (int ks = 0; ks < N / 16; ++ks) {
-          const uint32_t aoff = (ks / 4) * (MR * 128) + (ks % 4) * 32;
-          mma_f16(tmem + Cfg::COL_YI, smem_desc(saddr(Ct) + aoff, 16, 1024, kSwizzle128B),
-                  smem_desc(saddr(Rt) + ks * 2048, N * 128, 1024, kSwizzle128B), idesc, ks > 0);
-        }
-      }
-      {
-        constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
+          for (int q = 0; q < 2; ++q) {
+            float ta[16], tb[16];
+            tmem_ld16(tmem + lane_base + Cfg::COL_Y + s * P + 32 * half + 16 * q, ta);
+            tmem_ld16(tmem + lane_base + Cfg::COL_YI + s * P + 32 * half + 16 * q, tb);
 #pragma unroll
-        for (int ks = 0; ks < MR / 16; ++ks) {
-          mma_f16(tmem + Cfg::COL_G, smem_desc(saddr(Bt) + ks * 2048, MR * 128, 1024, kSwizzle128B),
-                  smem_desc(saddr(WXt) + ks * 2048, MR * 128, 1024, kSwizzle128B), idesc, 1);
-        }
-      }
-      mma_commit(saddr(&mma_bar));
-    }
-    {
-      const bool got = mbar_wait(saddr(&mma_bar), mma_phase, kMaxPolls);
-      mma_phase ^= 1;
-      if (!__syncthreads_and(got)) {
-        ok = false;
-        break;
-      }
-    }
-    tc_fence_after();
-
-    // ---- output: y = Y + e^{Lam_t} Yi + D x
-    {
-      const int t = acc_row_of(MR, warp, lane);
-      const int it = t >= 0 ? t / R : 0, rk = t >= 0 ? t % R : 0;
-      const bool valid = t >= 0 && it < nvalid;
-      const float el = sELam[it];
-      float* yrow = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
-      for (int cb = 0; cb < P; cb += 16) {
-        float a[16], b[16];
-        tmem_ld16(tmem + lane_base + Cfg::COL_Y + cb, a);
-        tmem_ld16(tmem + lane_base + Cfg::COL_YI + cb, b);
-        tmem_ld_wait();
-        if (valid) {
-          float o[16];
-#pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(Xt + sw128_offset(t, cb + 8 * hlf));
-            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xs[q]));
-              const int i0 = 8 * hlf + 2 * q;
-              o[i0] = fmaf(Dh, f.x, fmaf(el, b[i0], a[i0]));
-              o[i0 + 1] = fmaf(Dh, f.y, fmaf(el, b[i0 + 1], a[i0 + 1]));
+            for (int i = 0; i < 16; ++i) {
+              a[16 * q + i] = ta[i];
+              b[16 * q + i] = tb[i];
             }
           }
+          tmem_ld_wait();
+          if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(yrow + cb + 4 * q) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            for (int c8 = 0; c8 < 4; ++c8) {
+              const int col = 32 * half + 8 * c8;
+              const uint4 xv = *reinterpret_cast<const uint4*>(Xt + sw128_offset(t, col));
+              const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+              float o[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xs[q]));
+                const int i0 = 8 * c8 + 2 * q;
+                o[2 * q] = fmaf(Dh, f.x, fmaf(el, b[i0], a[i0]));
+                o[2 * q + 1] = fmaf(Dh, f.y, fmaf(el, b[i0 + 1], a[i0 + 1]));
+              }
+              *reinterpret_cast<float4*>(yrow + col) = make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(yrow + col + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            }
+          }
         }
       }
+      tc_fence_before();
+      group_sync(2, NSTA);
+      if (tt == 0) mbar_arrive(saddr(&bar_free[s]));
     }
-    tc_fence_before();
-    __syncthreads();
-  }
-
-  if (ok) {
-    tc_fence_after();
     // ---- final state (h of the last token) and carry (the last token's B and x)
-    if (p.h) {
-      const int n = g_row;
-      for (int cb = 0; cb < P; cb += 16) {
-        float v[16];
-        tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, v);
-        tmem_ld_wait();
-        if (n >= 0) {
-          float* hs = p.h + ((int64_t)unit * K2 + (n >> 1)) * P * 2 + (n & 1);
+    if (group_and(2, NSTA, wait_or_abort(saddr(&bar_gfull), (uint32_t)((nchunks - 1) & 1), abort_flag))) {
+      tc_fence_after();
+      if (p.h) {  // h = e^{i Phi_end} G' (pairs of rows are (re, im) in adjacent lanes)
+        float cs = 1.f, sn = 0.f;
+        if (g_row >= 0) sincosf(sPhi[g_row >> 1], &sn, &cs);
+        const bool re = (g_row & 1) == 0;
+        for (int cb = 0; cb < P; cb += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, v);
+          tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) hs[(cb + i) * 2] = v[i];
+          for (int i = 0; i < 16; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
+            v[i] = re ? (cs * v[i] - sn * other) : (sn * other + cs * v[i]);
+          }
+          if (g_row >= 0) {
+            float* hs = p.h + ((int64_t)unit * K2 + (g_row >> 1)) * P * 2 + (g_row & 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) hs[(cb + i) * 2] = v[i];
+          }
         }
       }
+      if (p.prev_B) {
+        const int64_t last = (tok0 + ntok - 1) * H + head;
+        for (int i = tt; i < R * N; i += NSTA) p.prev_B[(int64_t)unit * R * N + i] = p.B[last * R * N + i];
+        for (int i = tt; i < R * P; i += NSTA) p.prev_x[(int64_t)unit * R * P + i] = p.x[last * R * P + i];
+      }
     }
-    if (p.prev_B) {
-      const int64_t last = (tok0 + ntok - 1) * H + head;
-      for (int i = tid; i < R * N; i += NT) p.prev_B[(int64_t)unit * R * N + i] = p.B[last * R * N + i];
-      for (int i = tid; i < R * P; i += NT) p.prev_x[(int64_t)unit * R * P + i] = p.x[last * R * P + i];
+  } else if (warp == Cfg::W_MMA) {
+    // ======================= MMA warp (one thread issues)
+    if (lane == 0) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        uint8_t* stg = stage(s);
+        const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
+        const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
+        const uint32_t Xt = saddr(stg + Cfg::OFF_X), WXt = saddr(stg + Cfg::OFF_WX);
+        const uint32_t WXlo = saddr(stg + Cfg::OFF_WXLO);
+        if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
+        tc_fence_after();
+        // K-major operand tiles: 16-element K step = 32 B inside a 128 B row, 64-column blocks MR*128 B apart
+        auto kmaj = [](uint32_t base, int ks, uint32_t block_bytes) {
+          return smem_desc(base + (ks / 4) * block_bytes + (ks % 4) * 32, 16, 1024, kSwizzle128B);
+        };
+        // MN-major operand tiles: 16-element K step = two 8-row atoms
+        auto mnmaj = [](uint32_t base, int ks, uint32_t lbo) {
+          return smem_desc(base + ks * 2048, lbo, 1024, kSwizzle128B);
+        };
+        {  // MMA 1: S = C B^T = Chi Bhi^T + Chi Blo^T + Clo Bhi^T   (M = MR, N = MR, K = N)
+          constexpr uint32_t idesc = idesc_f16_f32(MR, MR, 0, 0);
+#pragma unroll
+          for (int ks = 0; ks < N / 16; ++ks) {
+            mma_f16(tmem + Cfg::COL_S, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, ks > 0);
+            mma_f16(tmem + Cfg::COL_S, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, MR * 128), idesc, 1);
+            mma_f16(tmem + Cfg::COL_S, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, 1);
+          }
+          mma_commit(saddr(&bar_sfull));
+        }
+        if (!wait_or_abort(saddr(&bar_spready), (uint32_t)(c & 1), abort_flag)) break;
+        if (c >= 2 && !wait_or_abort(saddr(&bar_free[s]), (uint32_t)(((c >> 1) - 1) & 1), abort_flag)) break;
+        tc_fence_after();
+        {  // MMA 2: Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16)
+          constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
+#pragma unroll
+          for (int ks = 0; ks < MR / 16; ++ks) {
+            mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(St), ks, MR * 128), mnmaj(Xt, ks, MR * 128), idesc, ks > 0);
+            mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(Stlo), ks, MR * 128), mnmaj(Xt, ks, MR * 128), idesc, 1);
+          }
+        }
+        if (!wait_or_abort(saddr(&bar_stready), (uint32_t)(c & 1), abort_flag)) break;
+        tc_fence_after();
+        {  // MMA 4: state += B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
+          constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
+#pragma unroll
+          for (int ks = 0; ks < MR / 16; ++ks) {
+            mma_f16(tmem + Cfg::COL_G, mnmaj(Bt, ks, MR * 128), mnmaj(WXt, ks, MR * 128), idesc, 1);
+            mma_f16(tmem + Cfg::COL_G, mnmaj(Bt, ks, MR * 128), mnmaj(WXlo, ks, MR * 128), idesc, 1);
+            mma_f16(tmem + Cfg::COL_G, mnmaj(Blo, ks, MR * 128), mnmaj(WXt, ks, MR * 128), idesc, 1);
+          }
+        }
+        {  // MMA 3: Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
+          constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
+#pragma unroll
+          for (int ks = 0; ks < N / 16; ++ks) {
+            mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Ct, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, ks > 0);
+            mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
+          }
+        }
+        // one commit covers every MMA issued so far: the state, R and the stage are released together
+        mma_commit(saddr(&bar_yfull));
+        mma_commit(saddr(&bar_gfull));
+        mma_commit(saddr(&bar_free[s]));
+      }
     }
   } else {
-    if (tid == 0) {
-      atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
-      // let loads still in flight land before the shared memory goes away
-      for (int s2 = 0; s2 < 2; ++s2)
-        if (issued[s2] > consumed[s2]) mbar_wait(saddr(&full_bar[s2]), (uint32_t)((issued[s2] - 1) & 1), kMaxPolls);
+    // ======================= TMA warp (one thread issues)
+    if (lane == 0) {
+      int issued[2] = {0, 0};
+      auto issue = [&](int c) {
+        const int s = c & 1;
+        uint8_t* stg = stage(s);
+        const uint32_t bar = saddr(&bar_full[s]);
+        const int t = (int)(tok0 + (int64_t)c * Q);
+        mbar_arrive_expect_tx(bar, Cfg::STAGE_TX);
+        tma_load_4d(saddr(stg + Cfg::OFF_X), &tm_x, bar, 0, 0, head, t);
+#pragma unroll
+        for (int kb = 0; kb < N / 64; ++kb) {
+          tma_load_4d(saddr(stg + Cfg::OFF_B + kb * MR * 128), &tm_B, bar, 64 * kb, 0, head, t);
+          tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head, t);
+        }
+        tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
+        issued[s] += 1;
+      };
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_B);
+      tma_prefetch_desc(&tm_C);
+      tma_prefetch_desc(&tm_th);
+      issue(0);
+      if (nchunks > 1) issue(1);
+      for (int c = 0; c + 2 < nchunks; ++c) {
+        if (!wait_or_abort(saddr(&bar_free[c & 1]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
+        issue(c + 2);
+      }
+      // every load issued must have landed before the CTA's shared memory goes away
+      for (int s = 0; s < 2; ++s)
+        if (issued[s] > 0) mbar_wait(saddr(&bar_full[s]), (uint32_t)((issued[s] - 1) & 1), kMaxPolls);
     }
   }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, Cfg::TMEM_COLS);
@@ -574,7 +717,7 @@ inline PFN_encodeTiled get_encode_tiled() {
   return fn;
 }
 
-// 3-D bf16 tensor [T][H][inner] (inner contiguous), box [Q][1][inner].
+// 3-D bf16 tensor [T][H][inner] (inner contiguous), box [Q][1][inner], unswizzled.
 inline bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H, uint64_t T, uint32_t Q) {
   PFN_encodeTiled enc = get_encode_tiled();
   if (!enc) return false;
@@ -587,14 +730,30 @@ inline bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D bf16 tensor [T][H][R][inner] (inner contiguous), box [Q][1][R][64] with
+// the 128-byte swizzle: each box lands as MR = Q*R rows of 128 B, exactly
+// one 64-column block of a 128B-swizzled operand tile.
+inline bool make_map_4d_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t R, uint64_t H,
+                              uint64_t T, uint32_t Q) {
+  PFN_encodeTiled enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {inner, R, H, T};
+  cuuint64_t strides[3] = {inner * 2, inner * R * 2, inner * R * H * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)R, 1, Q};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int N, int R, int Q>
 m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq, cudaStream_t s) {
   using Cfg = ChunkCfg<N, R, Q>;
   const int H = a->dims.nheads;
   const uint64_t T = (uint64_t)a->seqlen * (a->cu_seqlens ? 1 : a->dims.batch);
   CUtensorMap mx, mB, mC, mth;
-  if (!make_map_3d(&mx, a->x, (uint64_t)R * 64, H, T, Q) || !make_map_3d(&mB, a->B, (uint64_t)R * N, H, T, Q) ||
-      !make_map_3d(&mC, a->C, (uint64_t)R * N, H, T, Q) || !make_map_3d(&mth, a->theta, N / 2, H, T, Q))
+  if (!make_map_4d_sw128(&mx, a->x, 64, R, H, T, Q) || !make_map_4d_sw128(&mB, a->B, N, R, H, T, Q) ||
+      !make_map_4d_sw128(&mC, a->C, N, R, H, T, Q) || !make_map_3d(&mth, a->theta, N / 2, H, T, Q))
     return M3_ERR_CUDA;
   ChunkParams p{};
   p.x = static_cast<const __nv_bfloat16*>(a->x);
@@ -619,18 +778,18 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
 }
 
 // Shapes with a chunked kernel: bf16 inputs, P = 64, and (N, R, chunk) in
-// {(128, 1, 64), (64, 1, 64), (64, 4, 32), (64, 2, 32), (128, 2, 32)}.
+// {(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)}.
 inline m3_status chunked_prefill(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq,
                                  cudaStream_t s) {
   const m3_dims& d = a->dims;
   if (d.in_dtype != M3_BF16 || d.headdim != 64) return M3_ERR_UNSUPPORTED;
   const int R = d.rank, N = d.dstate;
-  const int Q = a->chunk > 0 ? a->chunk : (R == 1 ? 64 : 32);
+  const int Q = a->chunk > 0 ? a->chunk : (R == 1 ? 64 : 64 / R);
 #define M3_CH(NN, RR, QQ) \
   if (N == NN && R == RR && Q == QQ) return chunked_launch<NN, RR, QQ>(a, h, prev_B, prev_x, nseq, s);
   M3_CH(128, 1, 64)
   M3_CH(64, 1, 64)
-  M3_CH(64, 4, 32)
+  M3_CH(64, 4, 16)
   M3_CH(64, 2, 32)
   M3_CH(128, 2, 32)
 #undef M3_CH

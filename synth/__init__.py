@@ -129,7 +129,7 @@ def workloads() -> dict:
     w = {
         "tiny_f32": Workload("tiny_f32", "prefill", 1, 64, 2, 16, 16, 1, "f32", chunk=64),
         "siso_b8_l4096": Workload("siso_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16", chunk=64),
-        "mimo4_b8_l4096": Workload("mimo4_b8_l4096", "prefill", 8, 4096, 32, 64, 64, 4, "bf16", chunk=32),
+        "mimo4_b8_l4096": Workload("mimo4_b8_l4096", "prefill", 8, 4096, 32, 64, 64, 4, "bf16", chunk=16),
         "decode_siso_b256": Workload(
             "decode_siso_b256", "decode", 256, 1024, 32, 64, 128, 1, "bf16", h0_std=0.1, carry=True
         ),

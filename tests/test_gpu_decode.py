@@ -23,6 +23,7 @@ def run_decode(wl, steps, units=None, window=None):
     ys = []
     sel = list(range(b * H)) if units is None else list(units)
     y = torch.empty((b, H, R, P), dtype=torch.float32, device="cuda")
+    sumsq = torch.zeros((), dtype=torch.float64, device="cuda")  # over every unit and step
     allin = {}
     for s0 in range(0, steps, window):
         n = min(window, steps - s0)
@@ -32,6 +33,7 @@ def run_decode(wl, steps, units=None, window=None):
         for i in range(n):
             m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], t["lam"][i], t["theta"][i],
                               A, D, y, st)
+            sumsq += (y.double() ** 2).sum()
             ys.append(y.reshape(b * H, R, P)[sel].cpu().numpy())
         for k in ("x", "B", "C", "dt", "lam", "theta"):
             v = d[k].reshape((n, b * H) + d[k].shape[3:])[:, sel] if k not in ("dt", "lam") else \
@@ -40,7 +42,9 @@ def run_decode(wl, steps, units=None, window=None):
     torch.cuda.synchronize()
     assert m3.m3_device_status() == m3.M3_OK
     h, pB, px = st.views()
-    gpu = dict(y=np.stack(ys), h=to_np(h).reshape(b * H, N // 2, P, 2)[sel],
+    gpu = dict(y=np.stack(ys), y_rms=float(torch.sqrt(sumsq / (steps * y.numel())).item()),
+               h_rms=float(torch.sqrt((h.double() ** 2).mean()).item()),
+               h=to_np(h).reshape(b * H, N // 2, P, 2)[sel],
                pB=to_np(pB).reshape(b * H, R, N)[sel], px=to_np(px).reshape(b * H, R, P)[sel])
     st.free()
     # oracle over the sampled units only: pack them as a batch of len(sel) rows with one head each
@@ -68,9 +72,13 @@ def run_decode(wl, steps, units=None, window=None):
 
 
 def check(gpu, ref, dtype, what):
+    """max |err| over the checked units / rms over every unit (the GPU's
+    own outputs stand in for the reference rms: they differ by ~1e-6)."""
     tol = TOL[dtype]
-    assert_close(gpu["y"], ref["y"], tol, f"{what} y")
-    assert_close(gpu["h"], ref["h"], tol, f"{what} h_final")
+    ey = np.max(np.abs(gpu["y"] - ref["y"])) / gpu["y_rms"]
+    eh = np.max(np.abs(gpu["h"] - ref["h"])) / gpu["h_rms"]
+    assert ey <= tol, f"{what} y: max|err|/rms = {ey:.3e} > {tol:.1e}"
+    assert eh <= tol, f"{what} h_final: max|err|/rms = {eh:.3e} > {tol:.1e}"
     assert np.array_equal(gpu["pB"], ref["pB"]), f"{what} carry B"
     assert np.array_equal(gpu["px"], ref["px"]), f"{what} carry x"
 

@@ -43,7 +43,7 @@ def test_tiny_f32_config():
 
 SMALL = {
     "siso": dict(batch=2, seqlen=333, nheads=3, headdim=64, dstate=128, rank=1, chunk=64),
-    "mimo4": dict(batch=2, seqlen=201, nheads=3, headdim=64, dstate=64, rank=4, chunk=32),
+    "mimo4": dict(batch=2, seqlen=201, nheads=3, headdim=64, dstate=64, rank=4, chunk=16),
     "siso_long_dt": dict(batch=1, seqlen=517, nheads=2, headdim=64, dstate=128, rank=1, chunk=64, dt_shift=-3.0),
     "odd_shape": dict(batch=2, seqlen=45, nheads=2, headdim=32, dstate=48, rank=2, chunk=64),
 }
@@ -183,9 +183,10 @@ FULL = ["siso_b8_l4096", "mimo4_b8_l4096", "long_l16384", "varlen_16"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_units(name):
-    """Full-size workloads in the benchmark's launch configuration; the
-    oracle checks every token of sampled units (first, last, random)."""
+def test_full_size_every_output(name):
+    """Full-size workloads in the benchmark's launch configuration, every
+    output and every final state against the oracle (which finishes these
+    in seconds on the host cores): max |err| / rms over the whole tensor."""
     wl = synth.workloads()[name]
     inp = synth.prefill_inputs(wl)
     cu = wl.cu_seqlens if wl.kind == "varlen" else None
@@ -193,20 +194,14 @@ def test_full_size_sampled_units(name):
     st = state_for(dims_of(wl, batch=nseq))
     y = prefill_gpu(inp, wl, state=st, cu=cu)
     assert m3.m3_device_status() == m3.M3_OK
-    rng = np.random.default_rng(1)
-    U = nseq * wl.nheads
-    units = sorted(set([0, U - 1] + list(rng.choice(U, 6, replace=False))))
-    yo, ho, _, _, spans = oracle.prefill(inp, **oracle_kw(wl), cu_seqlens=cu, units=units)
-    yg = y.cpu().numpy()
+    yo, ho, _, _, _ = oracle.prefill(inp, **oracle_kw(wl), cu_seqlens=cu)
+    assert_close(y.cpu().numpy(), yo, TOL[wl.dtype], f"{name} y")
     h, _, _ = st.views()
-    hg = to_np(h).reshape((U,) + ho.shape[1:])
-    for i, (u, (b, t0, n, hd, _)) in enumerate(zip(units, spans)):
-        assert_close(yg[b, t0:t0 + n, hd], yo[u], TOL[wl.dtype], f"{name} unit {u} y")
-        assert_close(hg[u], ho[i], TOL[wl.dtype], f"{name} unit {u} h")
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL[wl.dtype], f"{name} h_final")
     st.free()
 
 
-CHUNKED_SHAPES = [(128, 1, 64), (64, 1, 64), (64, 4, 32), (64, 2, 32), (128, 2, 32)]
+CHUNKED_SHAPES = [(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)]
 
 
 @pytest.mark.parametrize("N,R,Q", CHUNKED_SHAPES)
