@@ -72,32 +72,44 @@ struct ChunkCfg {
   static constexpr int N = N_, R = R_, Q = Q_, P = 64;
   static constexpr int K2 = N / 2;  // complex pairs
   static constexpr int MR = Q * R;  // rows of S and Y: (token, rank)
-  static_assert(MR == 64 || MR == 128, "Q*R must be 64 or 128");
+  static_assert(MR == 64, "Q*R must be 64 (S and the outputs are double-buffered in TMEM)");
   static_assert(N == 64 || N == 128, "N must be 64 or 128");
-  // warp roles: 8 prologue warps, 4 state/output warps, 1 MMA warp, 1 TMA warp
-  static constexpr int NPRO = 256, NSTA = 128, NT = NPRO + NSTA + 64;
-  static constexpr int W_STA = NPRO / 32, W_MMA = W_STA + NSTA / 32, W_TMA = W_MMA + 1;
-  static_assert(NPRO % K2 == 0 && Q % (NPRO / K2) == 0, "angle-scan split");
-  // one chunk stage: TMA writes bf16 straight into the 128B-swizzled tiles
-  // of C, B (hi parts) and X, which the prologue converts to f16 in place
-  static constexpr int CT_BYTES = MR * N * 2;   // C, B tiles: [N/64 blocks][MR rows][128 B]
-  static constexpr int XT_BYTES = MR * P * 2;   // X, WX tiles: [MR rows][128 B]
-  static constexpr int TH_BYTES = Q * K2 * 2;   // theta [Q][K2] bf16 (unswizzled)
+  // warp roles: 8 prologue warps, 4 state/output warps, then one warp each
+  // for the intra-chunk MMAs (1 and 2), the TMA loads and the state-chain
+  // MMAs (4 and 3)
+  static constexpr int NPRO = 256, NSTA = 128, NT = NPRO + NSTA + 96;
+  static constexpr int W_STA = NPRO / 32, W_MMA = W_STA + NSTA / 32, W_TMA = W_MMA + 1, W_MMA2 = W_TMA + 1;
+  // rotation work split: consecutive threads take consecutive pairs (so
+  // shared-memory rows are read without bank conflicts), G token groups
+  static constexpr int G = NPRO / K2, TPG = Q / G;
+  static_assert(NPRO % K2 == 0 && Q % G == 0, "angle-scan split");
+  // one chunk stage.  TMA writes bf16 C and B straight into their (hi)
+  // 128B-swizzled operand tiles, which the prologue rotates and converts to
+  // f16 in place; x lands in the tile that then receives (W X) hi, theta in
+  // the area that then receives (W X) lo when it is large enough.
+  static constexpr int CT_BYTES = MR * N * 2;  // C, B tiles: [N/64 blocks][MR rows][128 B]
+  static constexpr int XT_BYTES = MR * P * 2;  // X, WX tiles: [MR rows][128 B]
+  static constexpr int TH_BYTES = Q * K2 * 2;  // theta [Q][K2] bf16 (unswizzled)
   static constexpr int OFF_C = 0, OFF_B = CT_BYTES, OFF_CLO = 2 * CT_BYTES, OFF_BLO = 3 * CT_BYTES;
-  static constexpr int OFF_X = 4 * CT_BYTES, OFF_WX = OFF_X + XT_BYTES;
-  static constexpr int OFF_TH = OFF_WX + XT_BYTES;
-  // the lo part of W X reuses the theta area when it is large enough (theta is dead by then)
+  static constexpr int OFF_X = 4 * CT_BYTES;  // x (bf16), then (W X) hi
+  static constexpr int OFF_TH = OFF_X + XT_BYTES;
   static constexpr bool WXLO_IN_TH = TH_BYTES >= XT_BYTES;
   static constexpr int OFF_WXLO = WXLO_IN_TH ? OFF_TH : align_up(OFF_TH + TH_BYTES, 1024);
   static constexpr int STAGE = align_up(WXLO_IN_TH ? OFF_TH + TH_BYTES : OFF_WXLO + XT_BYTES, 1024);
   static constexpr uint32_t STAGE_TX = 2 * CT_BYTES + XT_BYTES + TH_BYTES;
-  static constexpr int ST_BYTES = MR * MR * 2;  // S' hi and lo: [MR/64 blocks][MR rows][128 B], K-major
-  static constexpr int RT_BYTES = N * P * 2;    // R: [N rows][128 B], MN-major
-  static constexpr int OFF_ST = 2 * STAGE, OFF_STLO = OFF_ST + ST_BYTES, OFF_RT = OFF_STLO + ST_BYTES;
+  // outside the stages: X in f16 (it lives until the output of its chunk,
+  // so it and the per-chunk scalars rotate through XB slots: three when they
+  // fit), S' hi and lo (K-major), R (MN-major)
+  static constexpr int ST_BYTES = MR * MR * 2, RT_BYTES = N * P * 2;
+  static constexpr int smem_for(int xb) { return 2 * STAGE + xb * XT_BYTES + 2 * ST_BYTES + RT_BYTES + 1024; }
+  static constexpr int STATIC_EST = 3 * 6 * Q * 4 + (NPRO / K2) * K2 * 4 + 2048;  // scalars, scan, misc
+  static constexpr int XB = smem_for(3) + STATIC_EST <= 232448 ? 3 : 2;
+  static constexpr int OFF_XB = 2 * STAGE, OFF_ST = OFF_XB + XB * XT_BYTES, OFF_STLO = OFF_ST + ST_BYTES;
+  static constexpr int OFF_RT = OFF_STLO + ST_BYTES;
   static constexpr int SMEM = OFF_RT + RT_BYTES + 1024;  // + alignment slack
-  static_assert(SMEM + 6144 <= 232448, "shared memory of one CTA");
-  // TMEM columns (f32): S, Y[2], Yi[2], state
-  static constexpr int COL_S = 0, COL_Y = MR, COL_YI = MR + 2 * P, COL_G = MR + 4 * P;
+  static_assert(SMEM + STATIC_EST <= 232448, "shared memory of one CTA");
+  // TMEM columns (f32): S[2], Y[2], Yi[2], state
+  static constexpr int COL_S = 0, COL_Y = 2 * MR, COL_YI = 2 * MR + 2 * P, COL_G = 2 * MR + 4 * P;
   static constexpr int TMEM_COLS = 512;
   static_assert(COL_G + P <= TMEM_COLS, "TMEM columns");
 };
@@ -126,8 +138,8 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-// sin and cos of x after one reduction step by 2*pi (x stays within a few
-// hundred radians here), on the special-function unit.
+// sin and cos of x after one reduction step by 2*pi (|x| stays within a few
+// tens of radians here), on the special-function unit.
 __device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
   const float n = rintf(x * 0.15915494309189535f);
   __sincosf(fmaf(-n, 6.283185307179586f, x), s, c);
@@ -174,20 +186,24 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
                            const ChunkParams p) {
   using Cfg = ChunkCfg<N, R, Q>;
   constexpr int P = Cfg::P, K2 = Cfg::K2, MR = Cfg::MR, NPRO = Cfg::NPRO, NSTA = Cfg::NSTA;
-  constexpr int G = NPRO / K2, TPG = Q / G;  // angle scan: G token groups of TPG tokens
+  constexpr int G = Cfg::G, TPG = Cfg::TPG, XB = Cfg::XB;
   using namespace umma;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2];
-  __shared__ __align__(8) uint64_t bar_sfull, bar_spready, bar_stready, bar_yfull, bar_gfull;
+  // barriers: full (TMA landed), opready (prologue done), free (stage no longer
+  // read by MMAs), xfree (X buffer and output accumulators no longer read),
+  // sfull (MMA 1 done), yfull (MMAs 2 and 3 done), spready (S' written),
+  // stready (state step done), gfull (MMAs 4 and 3 done)
+  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_xfree[XB], bar_sfull[2], bar_yfull[2];
+  __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_gfull;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_abort[2];  // this CTA's abort flag; the status word at start
-  // per-chunk scalars, one set per stage
-  __shared__ float sLam[2][Q], sELam[2][Q], sGam[2][Q], sWp[2][Q], sDw[2][Q], sBw[2][Q], sLamEnd[2];
+  // per-chunk scalars, one set per X slot (chunk c uses slot c % XB)
+  __shared__ float sLam[XB][Q], sELam[XB][Q], sGam[XB][Q], sWp[XB][Q], sDw[XB][Q], sBw[XB][Q], sLamEnd[XB];
   // prologue scratch
   __shared__ float sDt[Q + 1], sBet[Q + 1], sWarpTot[4];
   __shared__ float sPsum[G][K2];
-  __shared__ float sPhi[K2];  // global angle per pair at the end of the last chunk, in [-pi, pi)
+  __shared__ float sPhi[K2];  // cumulative angle per pair at the end of the last chunk, in [-pi, pi)
 
   uint8_t* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -211,6 +227,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
   uint8_t* Stlo = sm + Cfg::OFF_STLO;
   uint8_t* Rt = sm + Cfg::OFF_RT;
   auto stage = [&](int s) { return sm + s * Cfg::STAGE; };
+  auto xbuf = [&](int x) { return sm + Cfg::OFF_XB + x * Cfg::XT_BYTES; };
+  // has the output of chunk cc (and its MMA 2) released X slot cc % XB?
+  auto wait_xfree = [&](int cc) {
+    return wait_or_abort(saddr(&bar_xfree[cc % XB]), (uint32_t)((cc / XB) & 1), abort_flag);
+  };
 
   if (tid == 0) {
     s_abort[0] = 0;
@@ -218,12 +239,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_full[s]), 1);
       mbar_init(saddr(&bar_opready[s]), 1);
-      mbar_init(saddr(&bar_free[s]), 2);  // output epilogue + MMA 4 completion
+      mbar_init(saddr(&bar_free[s]), 2);   // MMA 1 and MMAs 4/3 completions
+      mbar_init(saddr(&bar_sfull[s]), 1);
+      mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
     }
-    mbar_init(saddr(&bar_sfull), 1);
+    for (int x = 0; x < XB; ++x) mbar_init(saddr(&bar_xfree[x]), 2);  // MMA 2 completion and the output epilogue
     mbar_init(saddr(&bar_spready), 1);
     mbar_init(saddr(&bar_stready), 1);
-    mbar_init(saddr(&bar_yfull), 1);
     mbar_init(saddr(&bar_gfull), 1);
     mbar_init_fence();
   }
@@ -240,7 +262,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     // ======================= prologue warps: rotation, operands, S -> S'
     const int pt = tid;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const int k = pt % K2, g = pt / K2;
+    const int k = pt % K2, g = pt / K2;  // rotation: pair k for the tokens of group g
     if (pt < K2) sPhi[pt] = 0.f;
     // dt and lam of token pt of a chunk (token Q: the next chunk's first), loaded one chunk ahead
     auto load_scalars = [&](int c, float& d, float& l) {
@@ -256,17 +278,22 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     };
     float d_cur, l_cur;
     load_scalars(0, d_cur, l_cur);
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
+    // prologue of chunk c: scalars, angle scan, rotation of B and C, X and W X.
+    // Returns false when the pipeline was aborted.
+    auto prologue = [&](int c) -> bool {
+      const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
       float d_nxt, l_nxt;
       load_scalars(c + 1, d_nxt, l_nxt);
-      if (!group_and(1, NPRO, wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag))) break;
+      bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      // X slot xs (and its scalars) last served chunk c - XB: its output must be done
+      if (got && c >= XB) got = wait_xfree(c - XB);
+      if (!group_and(1, NPRO, got)) return false;
       // ---- per-token scalars and the inclusive scan of dt * A
       if (pt <= Q) {
         sDt[pt] = d_cur;
         sBet[pt] = (1.f - l_cur) * d_cur;
-        if (pt < Q) sGam[s][pt] = l_cur * d_cur;
+        if (pt < Q) sGam[xs][pt] = l_cur * d_cur;
       }
       // (whole warps take part in the shuffles: tokens Q..QW-1 contribute zero)
       constexpr int QW = (Q + 31) / 32 * 32;
@@ -280,37 +307,39 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         if (lane == 31) sWarpTot[warp] = v;
       }
       group_sync(1, NPRO);
+      if (pt < Q) {
+        for (int w = 0; w < warp; ++w) v += sWarpTot[w];
+        sLam[xs][pt] = v;
+      }
       // ---- angle scan, part 1: per-group sums of dt * theta
       const __nv_bfloat16* th = reinterpret_cast<const __nv_bfloat16*>(stg + Cfg::OFF_TH);
+      float om[TPG];
       {
         float part = 0.f;
-#pragma unroll 4
+#pragma unroll
         for (int ii = 0; ii < TPG; ++ii) {
           const int i = g * TPG + ii;
-          part = fmaf(sDt[i], __bfloat162float(th[i * K2 + k]), part);
+          om[ii] = sDt[i] * __bfloat162float(th[i * K2 + k]);
+          part += om[ii];
         }
         sPsum[g][k] = part;
       }
+      group_sync(1, NPRO);  // sLam and sPsum complete
+      const float lam_end = sLam[xs][Q - 1];
       if (pt < Q) {
-        for (int w = 0; w < warp; ++w) v += sWarpTot[w];
-        sLam[s][pt] = v;
-      }
-      group_sync(1, NPRO);
-      const float lam_end = sLam[s][Q - 1];
-      if (pt < Q) {
-        const float wp = sGam[s][pt] + sBet[pt + 1];
-        const float lt = sLam[s][pt];
-        sWp[s][pt] = wp;
-        sDw[s][pt] = __expf(lam_end - lt) * wp;
-        sBw[s][pt] = __expf(-lt) * wp;
-        sELam[s][pt] = __expf(lt);
-        if (pt == 0) sLamEnd[s] = lam_end;
+        const float wp = sGam[xs][pt] + sBet[pt + 1];
+        const float lt = sLam[xs][pt];
+        sWp[xs][pt] = wp;
+        sDw[xs][pt] = __expf(lam_end - lt) * wp;
+        sBw[xs][pt] = __expf(-lt) * wp;
+        sELam[xs][pt] = __expf(lt);
+        if (pt == 0) sLamEnd[xs] = lam_end;
       }
       // ---- angle scan, part 2, and the in-place rotation of B and C by
       //      e^{-i Phi_i}, Phi_i = phase at the chunk start + chunk-local sum
+      float tot = 0.f;
       {
-        const float phi0 = sPhi[k];
-        float off = 0.f, tot = 0.f;
+        float off = 0.f;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
           const float sv = sPsum[gg][k];
@@ -322,44 +351,53 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         uint8_t* Blo = stg + Cfg::OFF_BLO;
         uint8_t* Clo = stg + Cfg::OFF_CLO;
         const int blk = (2 * k) / 64, col = (2 * k) % 64;
-        float phi = phi0 + off;
-#pragma unroll 2
+        // angles of this thread's tokens, then all the sines and cosines,
+        // then the rotations: independent work the scheduler can overlap
+        float cs[TPG], sn[TPG];
+        {
+          float phi = sPhi[k] + off;
+#pragma unroll
+          for (int ii = 0; ii < TPG; ++ii) {
+            phi += om[ii];
+            cs[ii] = -phi;
+          }
+#pragma unroll
+          for (int ii = 0; ii < TPG; ++ii) sincos_reduced(cs[ii], &sn[ii], &cs[ii]);
+        }
+#pragma unroll
         for (int ii = 0; ii < TPG; ++ii) {
           const int i = g * TPG + ii;
-          phi = fmaf(sDt[i], __bfloat162float(th[i * K2 + k]), phi);
-          float sn, cs;
-          sincos_reduced(-phi, &sn, &cs);
 #pragma unroll
           for (int r = 0; r < R; ++r) {
             const uint32_t o = blk * (MR * 128) + sw128_offset(i * R + r, col);
             const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + o));
             const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
             uint32_t hi, lo;
-            split_half2(cs * b.x - sn * b.y, sn * b.x + cs * b.y, hi, lo);
+            split_half2(cs[ii] * b.x - sn[ii] * b.y, sn[ii] * b.x + cs[ii] * b.y, hi, lo);
             *reinterpret_cast<uint32_t*>(Bt + o) = hi;
             *reinterpret_cast<uint32_t*>(Blo + o) = lo;
-            split_half2(cs * cc.x - sn * cc.y, sn * cc.x + cs * cc.y, hi, lo);
+            split_half2(cs[ii] * cc.x - sn[ii] * cc.y, sn[ii] * cc.x + cs[ii] * cc.y, hi, lo);
             *reinterpret_cast<uint32_t*>(Ct + o) = hi;
             *reinterpret_cast<uint32_t*>(Clo + o) = lo;
           }
         }
-        group_sync(1, NPRO);  // sDw ready; every thread has read sPhi
-        if (g == 0) {         // advance the running phase by the chunk's angle, reduced to [-pi, pi)
-          const float ph = phi0 + tot;
-          sPhi[k] = fmaf(-rintf(ph * 0.15915494309189535f), 6.283185307179586f, ph);
-        }
       }
-      // ---- X to f16 in place, and W X
+      group_sync(1, NPRO);  // sDw ready; theta and sPhi fully read
+      if (g == 0) {         // advance the running phase by the chunk's angle, reduced to [-pi, pi)
+        const float ph = sPhi[k] + tot;
+        sPhi[k] = fmaf(-rintf(ph * 0.15915494309189535f), 6.283185307179586f, ph);
+      }
+      // ---- X to f16 (its own buffer) and W X as hi (over x) and lo parts
       {
-        uint8_t* Xt = stg + Cfg::OFF_X;
-        uint8_t* WXt = stg + Cfg::OFF_WX;
+        uint8_t* Xs = stg + Cfg::OFF_X;
         uint8_t* WXlo = stg + Cfg::OFF_WXLO;
+        uint8_t* Xb = xbuf(xs);
 #pragma unroll
         for (int idx = pt; idx < MR * (P / 8); idx += NPRO) {
           const int row = idx / (P / 8), c8 = idx % (P / 8);
           const uint32_t o = sw128_offset(row, c8 * 8);
-          const uint4 raw = *reinterpret_cast<const uint4*>(Xt + o);
-          const float w = sDw[s][row / R];
+          const uint4 raw = *reinterpret_cast<const uint4*>(Xs + o);
+          const float w = sDw[xs][row / R];
           const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t hx[4], hw[4], lw[4];
 #pragma unroll
@@ -368,8 +406,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
             hx[q] = pack_half2(f.x, f.y);
             split_half2(w * f.x, w * f.y, hw[q], lw[q]);
           }
-          *reinterpret_cast<uint4*>(Xt + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
-          *reinterpret_cast<uint4*>(WXt + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(Xb + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
+          *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
@@ -378,35 +416,45 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       if (pt == 0) mbar_arrive(saddr(&bar_opready[s]));
       d_cur = d_nxt;
       l_cur = l_nxt;
-
-      // ---- S -> S' once MMA 1 is done and MMA 2 of the previous chunk has read S'
-      bool got = wait_or_abort(saddr(&bar_sfull), (uint32_t)(c & 1), abort_flag);
-      if (got && c >= 1) got = wait_or_abort(saddr(&bar_yfull), (uint32_t)((c - 1) & 1), abort_flag);
-      if (!group_and(1, NPRO, got)) break;
+      return true;
+    };
+    // S -> S' of chunk c (after MMA 1 of c, and after MMA 2 of c - 1 has read S')
+    auto scores = [&](int c) -> bool {
+      const int s = c & 1, xs = c % XB;
+      const float lam_end = sLamEnd[xs];
+      bool got = wait_or_abort(saddr(&bar_sfull[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      if (got && c >= 1)
+        got = wait_or_abort(saddr(&bar_yfull[(c - 1) & 1]), (uint32_t)(((c - 1) >> 1) & 1), abort_flag);
+      if (!group_and(1, NPRO, got)) return false;
       tc_fence_after();
-      {
-        const int q4 = warp & 3;
-        const int t = acc_row_of(MR, q4, lane);
-        const int it = t >= 0 ? t / R : 0;
-        // last token held by this warp's rows: column blocks past it are all masked
-        const int it_warp = (MR == 128 ? 32 * q4 + 31 : 16 * q4 + 15) / R;
-        const float elam_t = sELam[s][it], lam_t = sLam[s][it], gam_t = sGam[s][it];
-        const bool factor = lam_end > -60.f;  // e^{Lam_t} and e^{-Lam_j} both stay normal floats
-        constexpr int CPH = MR / 2;           // columns per warp half
-        const int cbeg = (warp >> 2) * CPH;
-        float sv[CPH];
+      const int q4 = warp & 3;
+      const int t = acc_row_of(MR, q4, lane);
+      const int it = t >= 0 ? t / R : 0;
+      // last token held by this warp's rows: column blocks past it are all masked
+      const int it_warp = (16 * q4 + 15) / R;
+      const float elam_t = sELam[xs][it], lam_t = sLam[xs][it], gam_t = sGam[xs][it];
+      const bool factor = lam_end > -60.f;  // e^{Lam_t} and e^{-Lam_j} both stay normal floats
+      constexpr int CPH = MR / 2;           // columns per warp half
+      const int cbeg = (warp >> 2) * CPH;
+      float sv[CPH];
 #pragma unroll
-        for (int cb = 0; cb < CPH; cb += 16) {
-          float tmp[16];
-          if ((cbeg + cb) / R <= it_warp) tmem_ld16(tmem + lane_base + Cfg::COL_S + cbeg + cb, tmp);
+      for (int cb = 0; cb < CPH; cb += 16) {
+        float tmp[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sv[cb + i] = tmp[i];
-        }
-        tmem_ld_wait();
-        if (t >= 0) {
+        for (int i = 0; i < 16; ++i) tmp[i] = 0.f;
+        if ((cbeg + cb) / R <= it_warp) tmem_ld16(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, tmp);
 #pragma unroll
-          for (int cb = 0; cb < CPH; cb += 8) {
-            uint32_t hv[4], lv[4];
+        for (int i = 0; i < 16; ++i) sv[cb + i] = tmp[i];
+      }
+      tmem_ld_wait();
+      if (t >= 0) {
+#pragma unroll
+        for (int cb = 0; cb < CPH; cb += 8) {
+          uint32_t hv[4], lv[4];
+          if ((cbeg + cb) / R > it) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hv[q] = lv[q] = 0u;
+          } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float e[2];
@@ -415,25 +463,32 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
                 const int j = cbeg + cb + 2 * q + u, jt = j / R;
                 float val;
                 if (jt < it)
-                  val = factor ? sv[cb + 2 * q + u] * sBw[s][jt] * elam_t
-                               : sv[cb + 2 * q + u] * __expf(lam_t - sLam[s][jt]) * sWp[s][jt];
+                  val = factor ? sv[cb + 2 * q + u] * sBw[xs][jt] * elam_t
+                               : sv[cb + 2 * q + u] * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
                 else
                   val = (jt == it) ? sv[cb + 2 * q + u] * gam_t : 0.f;
                 e[u] = val;
               }
               split_half2(e[0], e[1], hv[q], lv[q]);
             }
-            const int j = cbeg + cb;
-            const uint32_t o = (j / 64) * (MR * 128) + sw128_offset(t, j % 64);
-            *reinterpret_cast<uint4*>(St + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            *reinterpret_cast<uint4*>(Stlo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
           }
+          const int j = cbeg + cb;
+          const uint32_t o = (j / 64) * (MR * 128) + sw128_offset(t, j % 64);
+          *reinterpret_cast<uint4*>(St + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(Stlo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
         }
       }
       tc_fence_before();
       fence_async_smem();
       group_sync(1, NPRO);
       if (pt == 0) mbar_arrive(saddr(&bar_spready));
+      return true;
+    };
+    // the prologue runs one chunk ahead of S -> S', which waits for MMA 1
+    bool alive = prologue(0);
+    for (int c = 0; c < nchunks && alive; ++c) {
+      if (c + 1 < nchunks && !prologue(c + 1)) break;
+      alive = scores(c);
     }
   } else if (warp < Cfg::W_MMA) {
     // ======================= state warps: state step and output epilogue
@@ -468,98 +523,105 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       }
       tmem_st_wait();
     }
-    bool alive = true;
-    for (int c = 0; c < nchunks && alive; ++c) {
-      const int s = c & 1;
-      uint8_t* stg = stage(s);
-      const int64_t ct0 = tok0 + (int64_t)c * Q;
-      const int nvalid = (ntok - (int64_t)c * Q < Q) ? (int)(ntok - (int64_t)c * Q) : Q;
+    // state step of chunk c: needs its scalars (prologue) and the state after MMA 4 of chunk c-1
+    auto state_step = [&](int c) -> bool {
+      const int s = c & 1, xs = c % XB;
       bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       if (got && c >= 1) got = wait_or_abort(saddr(&bar_gfull), (uint32_t)((c - 1) & 1), abort_flag);
-      if (!group_and(2, NSTA, got)) break;
+      if (!group_and(2, NSTA, got)) return false;
       tc_fence_after();
-      // ---- state step (rotating frame): R = G' as the f16 operand of MMA 3, G' <- e^{Lam_end} G'
-      {
-        const float elam_end = __expf(sLamEnd[s]);
-        float v[P];
+      // rotating frame: R = G' is the f16 operand of MMA 3, then G' <- e^{Lam_end} G'
+      const float elam_end = __expf(sLamEnd[xs]);
+      float v[P];
 #pragma unroll
-        for (int cb = 0; cb < P; cb += 16) {
-          float tmp[16];
-          tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, tmp);
+      for (int cb = 0; cb < P; cb += 16) {
+        float tmp[16];
+        tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, tmp);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[cb + i] = tmp[i];
-        }
-        tmem_ld_wait();
-        if (g_row >= 0) {
-#pragma unroll
-          for (int pc = 0; pc < P; pc += 8) {
-            const uint32_t o = sw128_offset(g_row, pc);
-            *reinterpret_cast<uint4*>(Rt + o) =
-                make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
-                           pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
-          }
-        }
-#pragma unroll
-        for (int cb = 0; cb < P; cb += 16) {
-          float tmp[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) tmp[i] = v[cb + i] * elam_end;
-          tmem_st16(tmem + lane_base + Cfg::COL_G + cb, tmp);
-        }
-        tmem_st_wait();
+        for (int i = 0; i < 16; ++i) v[cb + i] = tmp[i];
       }
+      tmem_ld_wait();
+      if (g_row >= 0) {
+#pragma unroll
+        for (int pc = 0; pc < P; pc += 8) {
+          const uint32_t o = sw128_offset(g_row, pc);
+          *reinterpret_cast<uint4*>(Rt + o) =
+              make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
+                         pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
+        }
+      }
+#pragma unroll
+      for (int cb = 0; cb < P; cb += 16) {
+        float tmp[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) tmp[i] = v[cb + i] * elam_end;
+        tmem_st16(tmem + lane_base + Cfg::COL_G + cb, tmp);
+      }
+      tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       group_sync(2, NSTA);
       if (tt == 0) mbar_arrive(saddr(&bar_stready));
-      // ---- output: y = Y + e^{Lam_t} Yi + D x
-      if (!group_and(2, NSTA, wait_or_abort(saddr(&bar_yfull), (uint32_t)(c & 1), abort_flag))) break;
+      return true;
+    };
+    // output of chunk c: y = Y + e^{Lam_t} Yi + D x, needs MMAs 2 and 3 of chunk c
+    auto output = [&](int c) -> bool {
+      const int s = c & 1, xs = c % XB;
+      const int64_t ct0 = tok0 + (int64_t)c * Q;
+      const int nvalid = (ntok - (int64_t)c * Q < Q) ? (int)(ntok - (int64_t)c * Q) : Q;
+      if (!group_and(2, NSTA, wait_or_abort(saddr(&bar_yfull[s]), (uint32_t)((c >> 1) & 1), abort_flag)))
+        return false;
       tc_fence_after();
-      {
-        const uint8_t* Xt = stg + Cfg::OFF_X;
-        const int t = acc_row_of(MR, q4, lane);
-        const int it = t >= 0 ? t / R : 0, rk = t >= 0 ? t % R : 0;
-        const bool valid = t >= 0 && it < nvalid;
-        const float el = sELam[s][it];
-        float* yrow = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
+      const uint8_t* Xb = xbuf(xs);
+      const int t = acc_row_of(MR, q4, lane);
+      const int it = t >= 0 ? t / R : 0, rk = t >= 0 ? t % R : 0;
+      const bool valid = t >= 0 && it < nvalid;
+      const float el = sELam[xs][it];
+      float* yrow = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float a[32], b[32];
+      for (int half = 0; half < 2; ++half) {
+        float a[32], b[32];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            float ta[16], tb[16];
-            tmem_ld16(tmem + lane_base + Cfg::COL_Y + s * P + 32 * half + 16 * q, ta);
-            tmem_ld16(tmem + lane_base + Cfg::COL_YI + s * P + 32 * half + 16 * q, tb);
+        for (int q = 0; q < 2; ++q) {
+          float ta[16], tb[16];
+          tmem_ld16(tmem + lane_base + Cfg::COL_Y + s * P + 32 * half + 16 * q, ta);
+          tmem_ld16(tmem + lane_base + Cfg::COL_YI + s * P + 32 * half + 16 * q, tb);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              a[16 * q + i] = ta[i];
-              b[16 * q + i] = tb[i];
-            }
+          for (int i = 0; i < 16; ++i) {
+            a[16 * q + i] = ta[i];
+            b[16 * q + i] = tb[i];
           }
-          tmem_ld_wait();
-          if (valid) {
+        }
+        tmem_ld_wait();
+        if (valid) {
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              const int col = 32 * half + 8 * c8;
-              const uint4 xv = *reinterpret_cast<const uint4*>(Xt + sw128_offset(t, col));
-              const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-              float o[8];
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const int col = 32 * half + 8 * c8;
+            const uint4 xv = *reinterpret_cast<const uint4*>(Xb + sw128_offset(t, col));
+            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+            float o[8];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xs[q]));
-                const int i0 = 8 * c8 + 2 * q;
-                o[2 * q] = fmaf(Dh, f.x, fmaf(el, b[i0], a[i0]));
-                o[2 * q + 1] = fmaf(Dh, f.y, fmaf(el, b[i0 + 1], a[i0 + 1]));
-              }
-              *reinterpret_cast<float4*>(yrow + col) = make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(yrow + col + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            for (int q = 0; q < 4; ++q) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xs[q]));
+              const int i0 = 8 * c8 + 2 * q;
+              o[2 * q] = fmaf(Dh, f.x, fmaf(el, b[i0], a[i0]));
+              o[2 * q + 1] = fmaf(Dh, f.y, fmaf(el, b[i0 + 1], a[i0 + 1]));
             }
+            *reinterpret_cast<float4*>(yrow + col) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(yrow + col + 4) = make_float4(o[4], o[5], o[6], o[7]);
           }
         }
       }
       tc_fence_before();
       group_sync(2, NSTA);
-      if (tt == 0) mbar_arrive(saddr(&bar_free[s]));
+      if (tt == 0) mbar_arrive(saddr(&bar_xfree[xs]));
+      return true;
+    };
+    // the state step runs one chunk ahead of the output
+    bool alive = state_step(0);
+    for (int c = 0; c < nchunks && alive; ++c) {
+      if (c + 1 < nchunks && !state_step(c + 1)) break;
+      alive = output(c);
     }
     // ---- final state (h of the last token) and carry (the last token's B and x)
     if (group_and(2, NSTA, wait_or_abort(saddr(&bar_gfull), (uint32_t)((nchunks - 1) & 1), abort_flag))) {
@@ -590,50 +652,69 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         for (int i = tt; i < R * P; i += NSTA) p.prev_x[(int64_t)unit * R * P + i] = p.x[last * R * P + i];
       }
     }
-  } else if (warp == Cfg::W_MMA) {
-    // ======================= MMA warp (one thread issues)
-    if (lane == 0) {
+  } else if (warp == Cfg::W_MMA || warp == Cfg::W_MMA2) {
+    // ======================= MMA warps (one thread each issues)
+    // K-major operand tiles: 16-element K step = 32 B inside a 128 B row, 64-column blocks MR*128 B apart
+    auto kmaj = [](uint32_t base, int ks, uint32_t block_bytes) {
+      return smem_desc(base + (ks / 4) * block_bytes + (ks % 4) * 32, 16, 1024, kSwizzle128B);
+    };
+    // MN-major operand tiles: 16-element K step = two 8-row atoms
+    auto mnmaj = [](uint32_t base, int ks, uint32_t lbo) {
+      return smem_desc(base + ks * 2048, lbo, 1024, kSwizzle128B);
+    };
+    if (lane == 0 && warp == Cfg::W_MMA) {
+      // intra-chunk products, MMA 1 one chunk ahead of MMA 2
+      auto mma1 = [&](int c) -> bool {
+        const int s = c & 1;
+        uint8_t* stg = stage(s);
+        const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
+        const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
+        if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) return false;
+        // S[s] was last read by S -> S' of chunk c - 2, which MMA 2 of chunk c - 2 already waited for
+        tc_fence_after();
+        // S = C B^T = Chi Bhi^T + Chi Blo^T + Clo Bhi^T   (M = MR, N = MR, K = N)
+        constexpr uint32_t idesc = idesc_f16_f32(MR, MR, 0, 0);
+        const uint32_t d = tmem + Cfg::COL_S + s * MR;
+#pragma unroll
+        for (int ks = 0; ks < N / 16; ++ks) {
+          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, ks > 0);
+          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, MR * 128), idesc, 1);
+          mma_f16(d, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, 1);
+        }
+        mma_commit(saddr(&bar_sfull[s]));
+        mma_commit(saddr(&bar_free[s]));
+        return true;
+      };
+      bool alive = mma1(0);
+      for (int c = 0; c < nchunks && alive; ++c) {
+        const int s = c & 1;
+        if (c + 1 < nchunks && !mma1(c + 1)) break;
+        if (!wait_or_abort(saddr(&bar_spready), (uint32_t)(c & 1), abort_flag)) break;
+        if (c >= 2 && !wait_xfree(c - 2)) break;  // Y[s] last held the output of chunk c - 2
+        tc_fence_after();
+        // Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16)
+        const uint32_t Xb = saddr(xbuf(c % XB));
+        constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < MR / 16; ++ks) {
+          mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(St), ks, MR * 128), mnmaj(Xb, ks, MR * 128), idesc, ks > 0);
+          mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(Stlo), ks, MR * 128), mnmaj(Xb, ks, MR * 128), idesc, 1);
+        }
+        mma_commit(saddr(&bar_yfull[s]));
+        mma_commit(saddr(&bar_xfree[c % XB]));
+      }
+    } else if (lane == 0) {
+      // state chain: MMA 4 (state update) and MMA 3 (inter-chunk output) of chunk c
       for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         uint8_t* stg = stage(s);
         const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
         const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
-        const uint32_t Xt = saddr(stg + Cfg::OFF_X), WXt = saddr(stg + Cfg::OFF_WX);
-        const uint32_t WXlo = saddr(stg + Cfg::OFF_WXLO);
-        if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
-        tc_fence_after();
-        // K-major operand tiles: 16-element K step = 32 B inside a 128 B row, 64-column blocks MR*128 B apart
-        auto kmaj = [](uint32_t base, int ks, uint32_t block_bytes) {
-          return smem_desc(base + (ks / 4) * block_bytes + (ks % 4) * 32, 16, 1024, kSwizzle128B);
-        };
-        // MN-major operand tiles: 16-element K step = two 8-row atoms
-        auto mnmaj = [](uint32_t base, int ks, uint32_t lbo) {
-          return smem_desc(base + ks * 2048, lbo, 1024, kSwizzle128B);
-        };
-        {  // MMA 1: S = C B^T = Chi Bhi^T + Chi Blo^T + Clo Bhi^T   (M = MR, N = MR, K = N)
-          constexpr uint32_t idesc = idesc_f16_f32(MR, MR, 0, 0);
-#pragma unroll
-          for (int ks = 0; ks < N / 16; ++ks) {
-            mma_f16(tmem + Cfg::COL_S, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, ks > 0);
-            mma_f16(tmem + Cfg::COL_S, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, MR * 128), idesc, 1);
-            mma_f16(tmem + Cfg::COL_S, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, 1);
-          }
-          mma_commit(saddr(&bar_sfull));
-        }
-        if (!wait_or_abort(saddr(&bar_spready), (uint32_t)(c & 1), abort_flag)) break;
-        if (c >= 2 && !wait_or_abort(saddr(&bar_free[s]), (uint32_t)(((c >> 1) - 1) & 1), abort_flag)) break;
-        tc_fence_after();
-        {  // MMA 2: Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16)
-          constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
-#pragma unroll
-          for (int ks = 0; ks < MR / 16; ++ks) {
-            mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(St), ks, MR * 128), mnmaj(Xt, ks, MR * 128), idesc, ks > 0);
-            mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(Stlo), ks, MR * 128), mnmaj(Xt, ks, MR * 128), idesc, 1);
-          }
-        }
+        const uint32_t WXt = saddr(stg + Cfg::OFF_X), WXlo = saddr(stg + Cfg::OFF_WXLO);
         if (!wait_or_abort(saddr(&bar_stready), (uint32_t)(c & 1), abort_flag)) break;
+        if (c >= 2 && !wait_xfree(c - 2)) break;  // Yi[s] last held the output of chunk c - 2
         tc_fence_after();
-        {  // MMA 4: state += B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
+        {  // state += B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
           constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
 #pragma unroll
           for (int ks = 0; ks < MR / 16; ++ks) {
@@ -642,7 +723,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
             mma_f16(tmem + Cfg::COL_G, mnmaj(Blo, ks, MR * 128), mnmaj(WXt, ks, MR * 128), idesc, 1);
           }
         }
-        {  // MMA 3: Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
+        {  // Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
           constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
 #pragma unroll
           for (int ks = 0; ks < N / 16; ++ks) {
@@ -650,16 +731,16 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
             mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
           }
         }
-        // one commit covers every MMA issued so far: the state, R and the stage are released together
-        mma_commit(saddr(&bar_yfull));
+        // one commit covers both products: the state, R, the output accumulator and the stage
         mma_commit(saddr(&bar_gfull));
+        mma_commit(saddr(&bar_yfull[s]));
         mma_commit(saddr(&bar_free[s]));
       }
     }
   } else {
     // ======================= TMA warp (one thread issues)
     if (lane == 0) {
-      int issued[2] = {0, 0};
+      int issued0 = 0, issued1 = 0;
       auto issue = [&](int c) {
         const int s = c & 1;
         uint8_t* stg = stage(s);
@@ -673,7 +754,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
           tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head, t);
         }
         tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
-        issued[s] += 1;
+        if (s) ++issued1; else ++issued0;
       };
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_B);
@@ -686,8 +767,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         issue(c + 2);
       }
       // every load issued must have landed before the CTA's shared memory goes away
-      for (int s = 0; s < 2; ++s)
-        if (issued[s] > 0) mbar_wait(saddr(&bar_full[s]), (uint32_t)((issued[s] - 1) & 1), kMaxPolls);
+      if (issued0 > 0) mbar_wait(saddr(&bar_full[0]), (uint32_t)((issued0 - 1) & 1), kMaxPolls);
+      if (issued1 > 0) mbar_wait(saddr(&bar_full[1]), (uint32_t)((issued1 - 1) & 1), kMaxPolls);
     }
   }
 
