@@ -191,15 +191,20 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
 
   extern __shared__ uint8_t smem_raw[];
   // barriers: full (TMA landed), opready (prologue done), free (stage no longer
-  // read by MMAs), xfree (X buffer and output accumulators no longer read),
-  // sfull (MMA 1 done), yfull (MMAs 2 and 3 done), spready (S' written),
-  // stready (state step done), gfull (MMAs 4 and 3 done)
-  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_xfree[XB], bar_sfull[2], bar_yfull[2];
+  // read by MMAs), xready (X of the slot's chunk converted), xfree (X slot and
+  // output accumulators no longer read), sfull (MMA 1 done), yfull (MMAs 2
+  // and 3 done), spready (S' written), stready (state step done), gfull
+  // (MMAs 4 and 3 done).  A phase-parity wait is only sound when the waiter
+  // can never fall two phases behind the barrier; each pairing below is
+  // chained so that it cannot.
+  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
+  __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB];
   __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_gfull;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_abort[2];  // this CTA's abort flag; the status word at start
   // per-chunk scalars, one set per X slot (chunk c uses slot c % XB)
-  __shared__ float sLam[XB][Q], sELam[XB][Q], sGam[XB][Q], sWp[XB][Q], sDw[XB][Q], sBw[XB][Q], sLamEnd[XB];
+  __shared__ float sLam[XB][Q], sELam[XB][Q], sGam[XB][Q], sWp[XB][Q], sDw[XB][Q], sLamEnd[XB];
+  __shared__ __align__(16) float sBw[XB][Q];
   // prologue scratch
   __shared__ float sDt[Q + 1], sBet[Q + 1], sWarpTot[4];
   __shared__ float sPsum[G][K2];
@@ -243,7 +248,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
     }
-    for (int x = 0; x < XB; ++x) mbar_init(saddr(&bar_xfree[x]), 2);  // MMA 2 completion and the output epilogue
+    for (int x = 0; x < XB; ++x) {
+      mbar_init(saddr(&bar_xfree[x]), 2);   // MMA 2 completion and the output epilogue
+      mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X
+    }
     mbar_init(saddr(&bar_spready), 1);
     mbar_init(saddr(&bar_stready), 1);
     mbar_init(saddr(&bar_gfull), 1);
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       float d_nxt, l_nxt;
       load_scalars(c + 1, d_nxt, l_nxt);
       bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
-      // X slot xs (and its scalars) last served chunk c - XB: its output must be done
+      // scalar slot xs last served chunk c - XB: its output must be done
       if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(1, NPRO, got)) return false;
       // ---- per-token scalars and the inclusive scan of dt * A
@@ -387,30 +395,6 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         const float ph = sPhi[k] + tot;
         sPhi[k] = fmaf(-rintf(ph * 0.15915494309189535f), 6.283185307179586f, ph);
       }
-      // ---- X to f16 (its own buffer) and W X as hi (over x) and lo parts
-      {
-        uint8_t* Xs = stg + Cfg::OFF_X;
-        uint8_t* WXlo = stg + Cfg::OFF_WXLO;
-        uint8_t* Xb = xbuf(xs);
-#pragma unroll
-        for (int idx = pt; idx < MR * (P / 8); idx += NPRO) {
-          const int row = idx / (P / 8), c8 = idx % (P / 8);
-          const uint32_t o = sw128_offset(row, c8 * 8);
-          const uint4 raw = *reinterpret_cast<const uint4*>(Xs + o);
-          const float w = sDw[xs][row / R];
-          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t hx[4], hw[4], lw[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = bf2_to_f2(rw[q]);
-            hx[q] = pack_half2(f.x, f.y);
-            split_half2(w * f.x, w * f.y, hw[q], lw[q]);
-          }
-          *reinterpret_cast<uint4*>(Xb + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
-          *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-      }
       fence_async_smem();
       group_sync(1, NPRO);
       if (pt == 0) mbar_arrive(saddr(&bar_opready[s]));
@@ -436,7 +420,15 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       const bool factor = lam_end > -60.f;  // e^{Lam_t} and e^{-Lam_j} both stay normal floats
       constexpr int CPH = MR / 2;           // columns per warp half
       const int cbeg = (warp >> 2) * CPH;
-      float sv[CPH];
+      float sv[CPH], bw[CPH / R];
+#pragma unroll
+      for (int q = 0; q < CPH / R; q += 4) {
+        const float4 w4 = *reinterpret_cast<const float4*>(&sBw[xs][cbeg / R + q]);
+        bw[q] = w4.x;
+        bw[q + 1] = w4.y;
+        bw[q + 2] = w4.z;
+        bw[q + 3] = w4.w;
+      }
 #pragma unroll
       for (int cb = 0; cb < CPH; cb += 16) {
         float tmp[16];
@@ -461,13 +453,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
 #pragma unroll
               for (int u = 0; u < 2; ++u) {
                 const int j = cbeg + cb + 2 * q + u, jt = j / R;
-                float val;
-                if (jt < it)
-                  val = factor ? sv[cb + 2 * q + u] * sBw[xs][jt] * elam_t
-                               : sv[cb + 2 * q + u] * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
-                else
-                  val = (jt == it) ? sv[cb + 2 * q + u] * gam_t : 0.f;
-                e[u] = val;
+                const float sij = sv[cb + 2 * q + u];
+                const float off = factor ? sij * bw[(cb + 2 * q + u) / R] * elam_t
+                                         : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
+                e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
               }
               split_half2(e[0], e[1], hv[q], lv[q]);
             }
@@ -526,9 +515,41 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     // state step of chunk c: needs its scalars (prologue) and the state after MMA 4 of chunk c-1
     auto state_step = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
+      uint8_t* stg = stage(s);
+      // X to f16 in slot xs (its previous chunk's MMA 2 and output are done)
+      // and W X as hi (over x) and lo parts: needs only the prologue, so it
+      // overlaps MMA 4 of the previous chunk
       bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
-      if (got && c >= 1) got = wait_or_abort(saddr(&bar_gfull), (uint32_t)((c - 1) & 1), abort_flag);
+      if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(2, NSTA, got)) return false;
+      {
+        uint8_t* Xs = stg + Cfg::OFF_X;
+        uint8_t* WXlo = stg + Cfg::OFF_WXLO;
+        uint8_t* Xb = xbuf(xs);
+#pragma unroll
+        for (int idx = tt; idx < MR * (P / 8); idx += NSTA) {
+          const int row = idx / (P / 8), c8 = idx % (P / 8);
+          const uint32_t o = sw128_offset(row, c8 * 8);
+          const uint4 raw = *reinterpret_cast<const uint4*>(Xs + o);
+          const float w = sDw[xs][row / R];
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hx[4], hw[4], lw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = bf2_to_f2(rw[q]);
+            hx[q] = pack_half2(f.x, f.y);
+            split_half2(w * f.x, w * f.y, hw[q], lw[q]);
+          }
+          *reinterpret_cast<uint4*>(Xb + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
+          *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        fence_async_smem();
+        group_sync(2, NSTA);
+        if (tt == 0) mbar_arrive(saddr(&bar_xready[xs]));
+      }
+      if (c >= 1 && !group_and(2, NSTA, wait_or_abort(saddr(&bar_gfull), (uint32_t)((c - 1) & 1), abort_flag)))
+        return false;
       tc_fence_after();
       // rotating frame: R = G' is the f16 operand of MMA 3, then G' <- e^{Lam_end} G'
       const float elam_end = __expf(sLamEnd[xs]);
@@ -690,6 +711,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         const int s = c & 1;
         if (c + 1 < nchunks && !mma1(c + 1)) break;
         if (!wait_or_abort(saddr(&bar_spready), (uint32_t)(c & 1), abort_flag)) break;
+        if (!wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;  // X of chunk c
         if (c >= 2 && !wait_xfree(c - 2)) break;  // Y[s] last held the output of chunk c - 2
         tc_fence_after();
         // Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16)
