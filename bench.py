@@ -88,53 +88,73 @@ def traffic_for(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
+    """SM clocks and throttle reasons sampled every few ms during a timed
+    region, read from the driver's NVML library through ctypes (reading
+    only; no setting is touched)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_CLOCK_SM = 1
+    REASONS = {
+        "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+    }
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+    def __init__(self, cuda_index: int, period_s: float = 0.005):
+        self.idx, self.period = cuda_index, period_s
+        self.samples, self.max_mhz, self.err = [], None, None
+
+    def _open(self):
+        import ctypes
+
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.idx)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle for " + bus.decode())
+        self.lib, self.h, self.ct = lib, h, ctypes
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        self.get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
 
     def __enter__(self):
+        import threading
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+            self._open()
+        except Exception as e:  # pragma: no cover - depends on the box
+            self.err = repr(e)[:120]
+            return self
+        self.stop = threading.Event()
+        ct, lib, h = self.ct, self.lib, self.h
+
+        def run():
+            sm, rs = ct.c_uint(), ct.c_ulonglong()
+            while not self.stop.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ct.byref(sm)) == 0 and \
+                        self.get_reasons(h, ct.byref(rs)) == 0:
+                    self.samples.append((sm.value, rs.value))
+                self.stop.wait(self.period)
+
+        self.th = threading.Thread(target=run, daemon=True)
+        self.th.start()
         return self
 
     def __exit__(self, *a):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.f.close()
+        if self.err is None:
+            self.stop.set()
+            self.th.join(timeout=2)
 
     def summary(self):
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        if self.err is not None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [self.err or "no samples"]}
+        sm = [x for x, _ in self.samples]
+        reasons = sorted({n for _, r in self.samples for n, bit in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "sm_mhz_min": min(sm)}
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -222,83 +242,53 @@ def config_of(wl):
 # ------------------------------------------------------------------ GPU arm
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="siso_b8_l4096")
-    ap.add_argument("--algo", default="auto", choices=["auto", "recurrent", "chunked"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    wl = synth.workloads()[args.workload]
-    if args.impl == "reference":
-        return run_reference(args, wl)
+def dev_tensor(torch, a):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.bfloat16)
+    return t.cuda()
 
-    import torch
-    import torch.distributed as dist
 
-    import state_space_sequence_06_b300 as m3
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
+def measure(wl, args, m3, torch, dist, world, local, stream, headline):
+    """Time `args.steps` passes of `wl` after `args.warmup` untimed ones.
+    Returns the JSON fields for it (the headline also gets e2e, the CPU
+    oracle baseline and a sampled parity check)."""
     algo = {"auto": m3.M3_ALGO_AUTO, "recurrent": m3.M3_ALGO_RECURRENT, "chunked": m3.M3_ALGO_CHUNKED}[args.algo]
-    hbm_peak, tc_peak, peak_src = peaks()
-    stream = torch.cuda.current_stream()
-
-    def dev(a):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        if a.dtype == np.uint16:
-            t = t.view(torch.bfloat16)
-        return t.cuda()
-
+    hbm_peak, _, peak_src = peaks()
     dims_dtype = m3.M3_BF16 if wl.dtype == "bf16" else m3.M3_F32
     H, P, N, R = wl.nheads, wl.headdim, wl.dstate, wl.rank
     byt = workload_bytes(wl)
     ev_pairs = []
+    cu = None
 
     if wl.kind == "decode":
         d = synth.decode_inputs(wl)
         T = wl.seqlen
-        t = {k: dev(d[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
-        A, D = t["A"], t["D"]
+        t = {k: dev_tensor(torch, d[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
         st = m3.m3_state_alloc(m3.make_dims(wl.batch, H, P, N, R, dims_dtype))
         hv, pB, px = st.views()
-        h0 = dev(d["h0"])
-        pB0, px0 = dev(d["prev_B"]), dev(d["prev_x"])
+        h0, pB0, px0 = dev_tensor(torch, d["h0"]), dev_tensor(torch, d["prev_B"]), dev_tensor(torch, d["prev_x"])
         y = torch.empty((wl.batch, H, R, P), dtype=torch.float32, device="cuda")
+        del d
 
         def step():
-            hv.copy_(h0)  # every pass starts from the same initial state
+            hv.copy_(h0)  # every pass starts from the same initial state and carry
             pB.copy_(pB0)
             px.copy_(px0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for i in range(T):
                 m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], t["lam"][i], t["theta"][i],
-                                  A, D, y, st)
+                                  t["A"], t["D"], y, st)
             e1.record(stream)
             ev_pairs.append((e0, e1))
 
-        launches_per_step = T
-        units_per_step = T  # decode steps
-        unit_name = "steps/s"
+        launches_per_step, units_per_step, unit_name = T, T, "steps/s"
         kernel_key = f"decode_step:{wl.name}"
-        bytes_per_launch = byt["per_unit_of_work"]
-        h2d = sum(d[k].nbytes for k in ("x", "B", "C", "dt", "lam", "theta"))
-        d2h = T * y.numel() * 4
+        path_dtype = "f32"
     else:
         inp = synth.prefill_inputs(wl)
-        t = {k: dev(inp[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
-        cu = None
+        t = {k: dev_tensor(torch, inp[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
         nseq = wl.batch
         if wl.kind == "varlen":
             cu = torch.from_numpy(wl.cu_seqlens).cuda()
@@ -318,29 +308,25 @@ def main():
         units_per_step = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)  # tokens
         unit_name = "tokens/s"
         kernel_key = f"prefill:{wl.name}:{args.algo}"
-        bytes_per_launch = byt["per_unit_of_work"]
-        h2d = sum(inp[k].nbytes for k in ("x", "B", "C", "dt", "lam", "theta"))
-        d2h = y.numel() * 4
+        # which prefill kernel runs: the chunked one multiplies f16 operand
+        # pairs on the tensor cores (f32 accumulation); the recurrent one is f32
+        path_dtype = "f32"
+        if wl.dtype == "bf16" and algo != m3.M3_ALGO_RECURRENT:
+            try:
+                m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
+                                   state=st, cu_seqlens=cu, algo=m3.M3_ALGO_CHUNKED, chunk=wl.chunk)
+                path_dtype = "f16x2 (hi/lo f16 operands, f32 accumulate)"
+            except m3.M3Error as e:
+                if e.status != m3.M3_ERR_UNSUPPORTED:
+                    raise
+        torch.cuda.synchronize()
 
-    # which prefill kernel runs: the chunked one multiplies bf16 operands on
-    # the tensor cores (f32 accumulation); the recurrent one is f32 throughout
-    path_dtype = "f32"
-    if wl.kind != "decode" and wl.dtype == "bf16" and algo != m3.M3_ALGO_RECURRENT:
-        try:
-            m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                               state=st, cu_seqlens=cu, algo=m3.M3_ALGO_CHUNKED, chunk=wl.chunk)
-            path_dtype = "bf16"
-        except m3.M3Error as e:
-            if e.status != m3.M3_ERR_UNSUPPORTED:
-                raise
-    torch.cuda.synchronize()
-
-    # quick sampled parity check of the timed configuration (oracle on 2 units)
     parity = None
-    try:
-        parity = sampled_parity(wl, m3, t, y, st, step if wl.kind == "decode" else None)
-    except Exception as e:  # reported, never hides a number
-        parity = {"error": repr(e)[:200]}
+    if headline and wl.kind != "decode":
+        try:
+            parity = sampled_parity(wl, m3, t, y, st, cu, algo)
+        except Exception as e:  # reported, never hides a number
+            parity = {"error": repr(e)[:200]}
 
     for _ in range(args.warmup):
         step()
@@ -366,87 +352,143 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
     kern_ms = [a.elapsed_time(b) for a, b in ev_pairs]
-    ms_per_step = total_ms / args.steps
-    value = units_per_step * args.steps * world / (total_ms / 1e3)
     status = m3.m3_device_status()
-
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the scan, D2H of y, all inside the timed region
-    e2e = None
-    if not args.no_e2e:
-        e2e = measure_e2e(wl, m3, torch, t, y, st, algo, args, world, stream)
-
+    # the dominant kernel's roofline: algorithmic bytes of one launch over its
+    # average duration (events on the launching stream)
     per_launch_ms = statistics.mean(kern_ms) / launches_per_step
-    achieved = bytes_per_launch / launches_per_step / (per_launch_ms / 1e3) / 1e9 if wl.kind != "decode" else \
-        bytes_per_launch / (per_launch_ms / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-            "traffic": traffic_for(kernel_key), "peak_source": peak_src,
-            "algorithmic_bytes_per_launch": bytes_per_launch / (1 if wl.kind != "decode" else 1),
-            "kernel_ms_per_launch": per_launch_ms}
+    bytes_per_launch = byt["per_unit_of_work"]  # one prefill pass, or one decode step
+    achieved = bytes_per_launch / (per_launch_ms / 1e3) / 1e9
+    out = {
+        "value": units_per_step * args.steps * world / (total_ms / 1e3), "unit": unit_name,
+        "ms_per_step": total_ms / args.steps, "dtype": path_dtype,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic_for(kernel_key),
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "kernel_ms_per_launch": per_launch_ms},
+        "gpu_launches": launches_per_step * args.steps, "device_status": status,
+        "clocks": clk.summary(), "parity": parity, "config": config_of(wl),
+    }
+    if headline and not args.no_e2e:
+        out["e2e"] = measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world)
+    st.free()
+    del t, y
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="siso_b8_l4096")
+    ap.add_argument("--algo", default="auto", choices=["auto", "recurrent", "chunked"])
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wls = synth.workloads()
+    wl = wls[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+
+    import state_space_sequence_06_b300 as m3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    stream = torch.cuda.current_stream()
+
+    head = measure(wl, args, m3, torch, dist, world, local, stream, headline=True)
+    others = []
+    if not args.quick:
+        for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "decode_siso_b256", "decode_mimo4_b256",
+                     "tiny_f32"):
+            if name == args.workload:
+                continue
+            sargs = argparse.Namespace(**vars(args))
+            if wls[name].kind == "decode":
+                sargs.steps = 2  # one step = the whole 1024-token decode loop
+            r = measure(wls[name], sargs, m3, torch, dist, world, local, stream, headline=False)
+            others.append({"workload": name, "value": r["value"], "unit": r["unit"], "ms_per_step": r["ms_per_step"],
+                           "dtype": r["dtype"], "roofline_frac": r["roofline"]["frac"],
+                           "achieved_gbs": r["roofline"]["achieved"],
+                           "kernel_ms_per_launch": r["roofline"]["kernel_ms_per_launch"],
+                           "gpu_launches": r["gpu_launches"], "device_status": r["device_status"],
+                           "clocks": r["clocks"]})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             r_, cores, sample = oracle_rate(wl, seconds=15.0)
-            cpu = {"value": r_, "unit": unit_name, "cores": cores, "kind": "oracle", "sample": sample}
+            cpu = {"value": r_, "unit": head["unit"], "cores": cores, "kind": "oracle", "sample": sample}
         except Exception as e:
             cpu = {"error": repr(e)[:200]}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": unit_name, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": path_dtype,
+            "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": head["dtype"],
             "data": "synthetic (seeded generator; shapes of the pages' 1.5B-scale workloads)",
-            "config": dict(config_of(wl), algo=args.algo,
-                           l2="inputs larger than L2 (%.2f GB per pass vs 126 MB L2)" % (bytes_per_launch / 1e9)
-                           if wl.kind != "decode" else "state larger than L2 (%.0f MB)" % (byt["state"] / 2 / 1e6),
+            "config": dict(head["config"], algo=args.algo,
+                           l2=("inputs larger than L2 (%.2f GB per pass vs 126 MB L2)"
+                               % (head["roofline"]["algorithmic_bytes_per_launch"] / 1e9)),
                            parallelism=f"replicas over independent units x{world}"),
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps, "device_status": status,
-            "clocks": clk.summary(), "parity": parity,
+            "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head.get("e2e"),
+            "gpu_launches": head["gpu_launches"], "device_status": head["device_status"],
+            "clocks": head["clocks"], "parity": head["parity"], "workloads": others,
         }
         print(json.dumps(line), flush=True)
-    st.free()
     if world > 1:
         dist.destroy_process_group()
 
 
-def sampled_parity(wl, m3, t, y, st, decode_step_fn):
-    """Compare two units of the timed configuration with the oracle."""
+def sampled_parity(wl, m3, t, y, st, cu, algo):
+    """Two units of the timed configuration against the oracle, max |err|
+    over them divided by the rms of the whole output tensor."""
     import torch
 
     import oracle
 
-    if wl.kind == "decode":
-        return None  # covered by tests/test_gpu_decode.py at full size
-    inp = synth.prefill_inputs(wl) if wl.kind != "decode" else None
-    cu = wl.cu_seqlens if wl.kind == "varlen" else None
-    nseq = wl.nseq if cu is not None else wl.batch
+    inp = synth.prefill_inputs(wl)
+    cu_np = wl.cu_seqlens if wl.kind == "varlen" else None
+    nseq = wl.nseq if cu_np is not None else wl.batch
     U = nseq * wl.nheads
     hv, pB, px = st.views()
     hv.zero_()
     pB.zero_()
     px.zero_()
     m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y, state=st,
-                       cu_seqlens=None if cu is None else torch.from_numpy(cu).cuda(), chunk=wl.chunk)
+                       cu_seqlens=cu, algo=algo, chunk=wl.chunk)
     torch.cuda.synchronize()
+    rms = float(torch.sqrt((y.double() ** 2).mean()).item())
     units = [0, U - 1]
     yo, ho, _, _, spans = oracle.prefill(inp, batch=wl.batch, L=wl.seqlen, H=wl.nheads, P=wl.headdim,
-                                         N=wl.dstate, R=wl.rank, dtype=wl.dtype, cu_seqlens=cu, units=units)
-    errs = []
+                                         N=wl.dstate, R=wl.rank, dtype=wl.dtype, cu_seqlens=cu_np, units=units)
+    err = 0.0
     for u, (b, t0, n, hd, _) in zip(units, spans):
         g = y[b, t0:t0 + n, hd].double().cpu().numpy()
-        r = yo[u]
-        errs.append(float(np.max(np.abs(g - r)) / np.sqrt(np.mean(r ** 2))))
+        err = max(err, float(np.max(np.abs(g - yo[u]))))
     hv.zero_()
     pB.zero_()
     px.zero_()
-    return {"units": units, "max_err_over_rms_y": max(errs)}
+    return {"units": units, "max_err_over_rms_y": err / rms}
 
 
-def measure_e2e(wl, m3, torch, t, y, st, algo, args, world, stream):
-    """Same metric through the public API from host buffers."""
+def measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world):
+    """The same metric through the public API from pinned host buffers: each
+    step copies its inputs host -> device, runs the scan and copies y back."""
     keys = ("x", "B", "C", "dt", "lam", "theta")
     host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in keys}
     for k in keys:
@@ -454,30 +496,16 @@ def measure_e2e(wl, m3, torch, t, y, st, algo, args, world, stream):
     yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
     torch.cuda.synchronize()
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
-    if wl.kind == "decode":
-        T = wl.seqlen
-        d2h = T * y.numel() * 4
-        yall = torch.empty((T,) + tuple(y.shape), dtype=y.dtype, pin_memory=True)
+    d2h = y.numel() * 4
+    units = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
 
-        def one():
-            for k in keys:
-                t[k].copy_(host[k], non_blocking=True)
-            for i in range(T):
-                m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], t["lam"][i], t["theta"][i],
-                                  t["A"], t["D"], y, st)
-                yall[i].copy_(y, non_blocking=True)
-        units = T
-    else:
-        d2h = y.numel() * 4
-        cu = torch.from_numpy(wl.cu_seqlens).cuda() if wl.kind == "varlen" else None
+    def one():
+        for k in keys:
+            t[k].copy_(host[k], non_blocking=True)
+        m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
+                           state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk)
+        yh.copy_(y, non_blocking=True)
 
-        def one():
-            for k in keys:
-                t[k].copy_(host[k], non_blocking=True)
-            m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                               state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk)
-            yh.copy_(y, non_blocking=True)
-        units = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
     steps = max(3, min(args.steps, 10))
     for _ in range(2):
         one()
@@ -487,8 +515,8 @@ def measure_e2e(wl, m3, torch, t, y, st, algo, args, world, stream):
         one()
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
-    return {"value": units * steps * world / el, "unit": "steps/s" if wl.kind == "decode" else "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    return {"value": units * steps * world / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
 
 
 if __name__ == "__main__":

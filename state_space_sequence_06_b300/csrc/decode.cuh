@@ -19,6 +19,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace m3 {
 
@@ -39,126 +40,194 @@ struct DecodeParams {
   int K;   // N / 2
   int PP;  // P / 2
   int KG;  // k groups (blockDim.x / PP)
+  int bulk;  // 1: every per-unit input row is a multiple of 16 bytes, so they arrive by bulk copy too
 };
 
 // R is the rank when known at compile time; R == 0 reads it from p.R (<= 8).
+//
+// The unit's state (K*P complex f32, 16-32 KB) moves HBM -> shared memory
+// with one bulk asynchronous copy (completing on an mbarrier) issued before
+// anything else, is updated in place, and goes back with one bulk copy: the
+// bytes in flight per SM are set by shared memory (several CTAs of 16-32 KB
+// each), not by registers.  Shared memory also holds, per pair k, a packed
+// record of float2 entries {a_k, Bprev_r[k], B_r[k], C_r[k] for r < R} (KW
+// float4 per pair) read with 128-bit broadcast loads (every lane of a warp
+// works on the same k); each thread keeps the x values of its two p columns
+// in registers.
 template <typename T, int ITEMS, int R_>
 __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) {
-  extern __shared__ float smem[];
+  using namespace umma;
+  extern __shared__ float4 smem4[];
+  __shared__ __align__(8) uint64_t bar;
   constexpr int RMAX = R_ > 0 ? R_ : 8;
+  constexpr int KW = (3 * RMAX + 2) / 2;  // float4 per pair record
   const int R = R_ > 0 ? R_ : p.R;
   const int K = p.K, N = p.N, P = p.P, PP = p.PP, KG = p.KG;
-  float2* alpha = reinterpret_cast<float2*>(smem);  // [K]
-  float* Bc = smem + 2 * K;                         // [R][N] this token's B
-  float* Bp = Bc + R * N;                           // [R][N] previous token's B
-  float* Cc = Bp + R * N;                           // [R][N]
-  float* xc = Cc + R * N;                           // [R][P]
-  float* xp = xc + R * P;                           // [R][P]
-  float* red = xp + R * P;                          // [KG][R][P]
+  float4* hsm = smem4;                                         // [K][PP]: the state, (re, im) x 2 per float4
+  float4* kd = hsm + (size_t)K * PP;                           // [K][KW]
+  float* xs = reinterpret_cast<float*>(kd + (size_t)K * KW);   // [2][R][P]: this token's x, previous x
+  float* red = xs + 2 * R * P;                                 // [KG][R][P]
+  // raw per-unit inputs, when they arrive by bulk copy: B, C, prev B [R][N], x, prev x [R][P], theta [K]
+  T* rawB = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(red + KG * R * P) + 15) & ~uintptr_t(15));
+  T* rawC = rawB + R * N;
+  T* rawPB = rawC + R * N;
+  T* rawX = rawPB + R * N;
+  T* rawPX = rawX + R * P;
+  T* rawTh = rawPX + R * P;
 
   const int unit = blockIdx.x;
   const int head = unit % p.H;
   const int tid = threadIdx.x;
   const int pp = tid % PP, kg = tid / PP;
+  float4* hg = reinterpret_cast<float4*>(p.h) + (int64_t)unit * K * PP;
+  const uint32_t state_bytes = (uint32_t)K * PP * 16;
 
-  // 1. issue the state loads first: they are the traffic that matters.
-  float4* hs = reinterpret_cast<float4*>(p.h) + (int64_t)unit * K * PP;
-  float4 hv[ITEMS];
-#pragma unroll
-  for (int i = 0; i < ITEMS; ++i) {
-    const int k = kg + i * KG;
-    if (k < K) hv[i] = ld_stream(hs + (int64_t)k * PP + pp);
-  }
-
-  // 2. stage the per-unit operands as f32.
   const T* xg = static_cast<const T*>(p.x) + (int64_t)unit * R * P;
   const T* Bg = static_cast<const T*>(p.B) + (int64_t)unit * R * N;
   const T* Cg = static_cast<const T*>(p.C) + (int64_t)unit * R * N;
   T* pBg = static_cast<T*>(p.prev_B) + (int64_t)unit * R * N;
   T* pxg = static_cast<T*>(p.prev_x) + (int64_t)unit * R * P;
+  const T* thg = static_cast<const T*>(p.theta) + (int64_t)unit * K;
+  const uint32_t rn_bytes = (uint32_t)(R * N * sizeof(T)), rp_bytes = (uint32_t)(R * P * sizeof(T));
+  const uint32_t th_bytes = (uint32_t)(K * sizeof(T));
+
+  // 1. start the copies first: the state is the traffic that matters, the
+  //    per-unit inputs ride on the same barrier when their rows allow it.
+  if (tid == 0) {
+    mbar_init(saddr(&bar), 1);
+    mbar_init_fence();
+    const uint32_t tx = state_bytes + (p.bulk ? 3 * rn_bytes + 2 * rp_bytes + th_bytes : 0u);
+    mbar_arrive_expect_tx(saddr(&bar), tx);
+    bulk_g2s(saddr(hsm), hg, state_bytes, saddr(&bar));
+    if (p.bulk) {
+      bulk_g2s(saddr(rawB), Bg, rn_bytes, saddr(&bar));
+      bulk_g2s(saddr(rawC), Cg, rn_bytes, saddr(&bar));
+      bulk_g2s(saddr(rawPB), pBg, rn_bytes, saddr(&bar));
+      bulk_g2s(saddr(rawX), xg, rp_bytes, saddr(&bar));
+      bulk_g2s(saddr(rawPX), pxg, rp_bytes, saddr(&bar));
+      bulk_g2s(saddr(rawTh), thg, th_bytes, saddr(&bar));
+    }
+  }
   const float dt = ldf(static_cast<const T*>(p.dt), unit);
   const float lam = ldf(static_cast<const T*>(p.lam), unit);
   const float A = p.A[head], D = p.D[head];
-  for (int i = tid; i < R * N; i += blockDim.x) {
-    Bc[i] = to_f(Bg[i]);
-    Bp[i] = to_f(pBg[i]);
-    Cc[i] = to_f(Cg[i]);
+  const float decay = expf(dt * A);
+  __syncthreads();  // the mbarrier initialisation is visible
+  // 2. wait for the copies (bounded), then stage the per-unit operands as f32 pair records.
+  bool landed = mbar_try_wait(saddr(&bar), 0);
+  for (uint32_t i = 0; !landed && i < (1u << 24); ++i) landed = mbar_try_wait(saddr(&bar), 0);
+  if (!__syncthreads_and(landed)) {
+    if (tid == 0) atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
+    return;
+  }
+  const T* sB = p.bulk ? rawB : Bg;
+  const T* sC = p.bulk ? rawC : Cg;
+  const T* sPB = p.bulk ? rawPB : pBg;
+  const T* sX = p.bulk ? rawX : xg;
+  const T* sPX = p.bulk ? rawPX : pxg;
+  const T* sTh = p.bulk ? rawTh : thg;
+  float2* kd2 = reinterpret_cast<float2*>(kd);
+  for (int i = tid; i < K * R; i += blockDim.x) {
+    const int k = i / R, r = i % R;
+    float2* rec = kd2 + (size_t)k * 2 * KW;
+    rec[1 + r] = make_float2(to_f(sPB[r * N + 2 * k]), to_f(sPB[r * N + 2 * k + 1]));
+    rec[1 + R + r] = make_float2(to_f(sB[r * N + 2 * k]), to_f(sB[r * N + 2 * k + 1]));
+    rec[1 + 2 * R + r] = make_float2(to_f(sC[r * N + 2 * k]), to_f(sC[r * N + 2 * k + 1]));
   }
   for (int i = tid; i < R * P; i += blockDim.x) {
-    xc[i] = to_f(xg[i]);
-    xp[i] = to_f(pxg[i]);
+    xs[i] = to_f(sX[i]);
+    xs[R * P + i] = to_f(sPX[i]);
   }
-  const float decay = expf(dt * A);
-  const T* thg = static_cast<const T*>(p.theta) + (int64_t)unit * K;
   for (int k = tid; k < K; k += blockDim.x) {
-    float s, c;
-    sincosf(dt * to_f(thg[k]), &s, &c);
-    alpha[k] = make_float2(decay * c, decay * s);
+    float sn, cs;
+    sincosf(dt * to_f(sTh[k]), &sn, &cs);
+    kd2[(size_t)k * 2 * KW] = make_float2(decay * cs, decay * sn);
   }
-  __syncthreads();
+  __syncthreads();  // records staged; the old carry is no longer needed
 
-  // 3. the carry becomes this token's (B, x); the old one is in smem now.
-  for (int i = tid; i < R * N; i += blockDim.x) pBg[i] = Bg[i];
-  for (int i = tid; i < R * P; i += blockDim.x) pxg[i] = xg[i];
+  // 3. the carry becomes this token's (B, x)
+  if (p.bulk) {
+    if (tid == 0) {  // straight from the staged copies
+      bulk_s2g(pBg, saddr(rawB), rn_bytes);
+      bulk_s2g(pxg, saddr(rawX), rp_bytes);
+      bulk_commit();
+    }
+  } else {
+    for (int i = tid; i < R * N; i += blockDim.x) pBg[i] = Bg[i];
+    for (int i = tid; i < R * P; i += blockDim.x) pxg[i] = xg[i];
+  }
 
-  // 4. update the owned entries and accumulate partial outputs.
+  // 4. update the owned entries in place and accumulate partial outputs.
   const float gam = lam * dt, bet = (1.f - lam) * dt;
-  float ypart[2 * RMAX];  // [R][2]
+  const int p0 = 2 * pp;
+  float xc0[RMAX], xc1[RMAX], xp0[RMAX], xp1[RMAX];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    const bool on = r < R;
+    xc0[r] = on ? xs[r * P + p0] : 0.f;
+    xc1[r] = on ? xs[r * P + p0 + 1] : 0.f;
+    xp0[r] = on ? xs[R * P + r * P + p0] : 0.f;
+    xp1[r] = on ? xs[R * P + r * P + p0 + 1] : 0.f;
+  }
+  float ypart[2 * RMAX];
 #pragma unroll
   for (int i = 0; i < 2 * RMAX; ++i) ypart[i] = 0.f;
-  const int p0 = 2 * pp;
-#pragma unroll
+#pragma unroll(R_ == 1 ? ITEMS : 1)
   for (int i = 0; i < ITEMS; ++i) {
     const int k = kg + i * KG;
     if (k < K) {
+      const float2* rec = kd2 + (size_t)k * 2 * KW;  // broadcast reads: every lane works on this k
       float ur0 = 0.f, ui0 = 0.f, ur1 = 0.f, ui1 = 0.f;  // u_prev at p0, p0+1
       float vr0 = 0.f, vi0 = 0.f, vr1 = 0.f, vi1 = 0.f;  // u_t at p0, p0+1
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         if (r >= R) break;
-        const float bpr = Bp[r * N + 2 * k], bpi = Bp[r * N + 2 * k + 1];
-        const float bcr = Bc[r * N + 2 * k], bci = Bc[r * N + 2 * k + 1];
-        const float xp0 = xp[r * P + p0], xp1 = xp[r * P + p0 + 1];
-        const float xc0 = xc[r * P + p0], xc1 = xc[r * P + p0 + 1];
-        ur0 = fmaf(bpr, xp0, ur0); ui0 = fmaf(bpi, xp0, ui0);
-        ur1 = fmaf(bpr, xp1, ur1); ui1 = fmaf(bpi, xp1, ui1);
-        vr0 = fmaf(bcr, xc0, vr0); vi0 = fmaf(bci, xc0, vi0);
-        vr1 = fmaf(bcr, xc1, vr1); vi1 = fmaf(bci, xc1, vi1);
+        const float2 bp = rec[1 + r], bc = rec[1 + R + r];
+        ur0 = fmaf(bp.x, xp0[r], ur0); ui0 = fmaf(bp.y, xp0[r], ui0);
+        ur1 = fmaf(bp.x, xp1[r], ur1); ui1 = fmaf(bp.y, xp1[r], ui1);
+        vr0 = fmaf(bc.x, xc0[r], vr0); vi0 = fmaf(bc.y, xc0[r], vi0);
+        vr1 = fmaf(bc.x, xc1[r], vr1); vi1 = fmaf(bc.y, xc1[r], vi1);
       }
-      const float2 a = alpha[k];
+      const float2 a = rec[0];
+      const float4 hv = hsm[(size_t)k * PP + pp];
       // g = h + bet * u_prev ; h' = a * g + gam * u_t
-      const float g0r = fmaf(bet, ur0, hv[i].x), g0i = fmaf(bet, ui0, hv[i].y);
-      const float g1r = fmaf(bet, ur1, hv[i].z), g1i = fmaf(bet, ui1, hv[i].w);
+      const float g0r = fmaf(bet, ur0, hv.x), g0i = fmaf(bet, ui0, hv.y);
+      const float g1r = fmaf(bet, ur1, hv.z), g1i = fmaf(bet, ui1, hv.w);
       float4 o;
       o.x = fmaf(a.x, g0r, fmaf(-a.y, g0i, gam * vr0));
       o.y = fmaf(a.x, g0i, fmaf(a.y, g0r, gam * vi0));
       o.z = fmaf(a.x, g1r, fmaf(-a.y, g1i, gam * vr1));
       o.w = fmaf(a.x, g1i, fmaf(a.y, g1r, gam * vi1));
-      st_stream(hs + (int64_t)k * PP + pp, o);
+      hsm[(size_t)k * PP + pp] = o;
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         if (r >= R) break;
-        const float cr = Cc[r * N + 2 * k], ci = Cc[r * N + 2 * k + 1];
-        ypart[2 * r] = fmaf(cr, o.x, fmaf(ci, o.y, ypart[2 * r]));
-        ypart[2 * r + 1] = fmaf(cr, o.z, fmaf(ci, o.w, ypart[2 * r + 1]));
+        const float2 cc = rec[1 + 2 * R + r];
+        ypart[2 * r] = fmaf(cc.x, o.x, fmaf(cc.y, o.y, ypart[2 * r]));
+        ypart[2 * r + 1] = fmaf(cc.x, o.z, fmaf(cc.y, o.w, ypart[2 * r + 1]));
       }
     }
   }
 
-  // 5. reduce the partial outputs over the KG groups.
+  // 5. write the state back (one bulk copy) and reduce the partial outputs.
 #pragma unroll
   for (int r = 0; r < RMAX; ++r) {
     if (r >= R) break;
-    red[(kg * R + r) * P + p0] = ypart[2 * r];
-    red[(kg * R + r) * P + p0 + 1] = ypart[2 * r + 1];
+    *reinterpret_cast<float2*>(&red[(kg * R + r) * P + p0]) = make_float2(ypart[2 * r], ypart[2 * r + 1]);
   }
+  fence_async_smem();
   __syncthreads();
+  if (tid == 0) {
+    bulk_s2g(hg, saddr(hsm), state_bytes);
+    bulk_commit();
+  }
   float* yg = p.y + (int64_t)unit * R * P;
   for (int i = tid; i < R * P; i += blockDim.x) {
-    float s = 0.f;
-    for (int g = 0; g < KG; ++g) s += red[g * R * P + i];
-    yg[i] = fmaf(D, xc[i], s);
+    float sum = 0.f;
+    for (int g = 0; g < KG; ++g) sum += red[g * R * P + i];
+    yg[i] = fmaf(D, xs[i], sum);
   }
+  if (tid == 0) bulk_wait_read_all();  // shared memory must outlive the copy's reads
 }
 
 }  // namespace m3

@@ -47,14 +47,22 @@ template <typename T, int ITEMS>
 m3_status decode_rank(const m3::DecodeParams& p, int threads, size_t smem, int units,
                       cudaStream_t s) {
   switch (p.R) {
-#define M3_DEC(RR)                                                                           \
-  case RR:                                                                                   \
-    m3::decode_step_kernel<T, ITEMS, RR><<<units, threads, smem, s>>>(p);                    \
+#define M3_DEC(RR)                                                                             \
+  case RR:                                                                                     \
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(m3::decode_step_kernel<T, ITEMS, RR>,          \
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                                 (int)smem) != cudaSuccess)                     \
+      return M3_ERR_CUDA;                                                                      \
+    m3::decode_step_kernel<T, ITEMS, RR><<<units, threads, smem, s>>>(p);                      \
     return launch_status();
     M3_DEC(1) M3_DEC(4)
 #undef M3_DEC
     default:
       if (p.R > 8) return M3_ERR_UNSUPPORTED;
+      if (smem > 48 * 1024 && cudaFuncSetAttribute(m3::decode_step_kernel<T, ITEMS, 0>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem) != cudaSuccess)
+        return M3_ERR_CUDA;
       m3::decode_step_kernel<T, ITEMS, 0><<<units, threads, smem, s>>>(p);
       return launch_status();
   }
@@ -65,13 +73,29 @@ m3_status decode_launch(m3::DecodeParams p, int units, cudaStream_t s) {
   p.K = p.N / 2;
   p.PP = p.P / 2;
   if (p.PP > 256) return M3_ERR_UNSUPPORTED;
-  int kg = 256 / p.PP;
+  // rank > 1 keeps more per-thread registers (x columns and outputs per
+  // rank): smaller CTAs keep more of them resident per SM
+  int kg = (p.R == 1 ? 256 : 128) / p.PP;
+  if (kg < 1) kg = 1;
+  while (ceil_div(p.K, kg) > 16 && p.PP * kg * 2 <= 256) kg *= 2;
   if (kg > p.K) kg = p.K;
   p.KG = kg;
   const int threads = p.PP * kg;
   int items = ceil_div(p.K, kg);
-  const size_t smem = sizeof(float) * (2 * p.K + 3 * p.R * p.N + 2 * p.R * p.P + kg * p.R * p.P);
-  if (smem > 48 * 1024) return M3_ERR_UNSUPPORTED;
+  // the state (K*P complex f32), pair records (KW float4 each, sized for the
+  // compile-time rank bound), x and previous x, partial outputs
+  const int rmax = p.R == 1 ? 1 : (p.R == 4 ? 4 : 8);
+  const size_t kw = (3 * rmax + 2) / 2;
+  const size_t esz = sizeof(T);
+  const size_t raw = esz * (3 * (size_t)p.R * p.N + 2 * (size_t)p.R * p.P + p.K);
+  auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  p.bulk = ((p.R * p.N * esz) % 16 == 0 && (p.R * p.P * esz) % 16 == 0 && (p.K * esz) % 16 == 0 &&
+            al16(p.x) && al16(p.B) && al16(p.C) && al16(p.theta) && al16(p.prev_B) && al16(p.prev_x))
+               ? 1
+               : 0;
+  const size_t smem = sizeof(float4) * p.K * (p.PP + kw) + sizeof(float) * (2 * p.R * p.P + kg * p.R * p.P) +
+                      (p.bulk ? raw + 16 : 0);
+  if (smem > 200 * 1024) return M3_ERR_UNSUPPORTED;
   if (items <= 1) return decode_rank<T, 1>(p, threads, smem, units, s);
   if (items <= 2) return decode_rank<T, 2>(p, threads, smem, units, s);
   if (items <= 4) return decode_rank<T, 4>(p, threads, smem, units, s);
