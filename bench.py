@@ -229,9 +229,25 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(torch, dist, world, value, device):
+    """The largest of every rank's `value` (the job's time is its slowest
+    rank's); timing only, no data of the scan crosses ranks."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step, steps, world, total_ms):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (total_ms / 1e3)
+
+
 def config_of(wl):
     c = {"workload": wl.name, "kind": wl.kind, "batch": wl.batch, "seq_len": wl.seqlen, "heads": wl.nheads,
-         "headdim": wl.headdim, "dstate": wl.dstate, "rank": wl.rank, "in_dtype": wl.dtype}
+         "headdim": wl.headdim, "dstate": wl.dstate, "mimo_rank": wl.rank, "in_dtype": wl.dtype,
+         "global_batch": (wl.nseq if wl.kind == "varlen" else wl.batch) * wl.shards}
     if wl.kind != "decode":
         c["chunk"] = wl.chunk
     if wl.kind == "varlen":
@@ -346,11 +362,7 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    total_ms = g0.elapsed_time(g1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(torch, dist, world, g0.elapsed_time(g1), "cuda")
     kern_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     status = m3.m3_device_status()
     # the dominant kernel's roofline: algorithmic bytes of one launch over its
@@ -359,7 +371,7 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
     bytes_per_launch = byt["per_unit_of_work"]  # one prefill pass, or one decode step
     achieved = bytes_per_launch / (per_launch_ms / 1e3) / 1e9
     out = {
-        "value": units_per_step * args.steps * world / (total_ms / 1e3), "unit": unit_name,
+        "value": job_rate(units_per_step, args.steps, world, total_ms), "unit": unit_name,
         "ms_per_step": total_ms / args.steps, "dtype": path_dtype,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic_for(kernel_key),
@@ -388,13 +400,19 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="decode workloads: tokens per pass (default: the workload's 1024); "
+                         "smaller passes keep profiler captures small")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wls = synth.workloads()
-    wl = wls[args.workload]
+    if args.decode_steps > 0:
+        for k, w in list(wls.items()):
+            if w.kind == "decode":
+                wls[k] = synth.scaled(w, seqlen=args.decode_steps)
     if args.impl == "reference":
-        return run_reference(args, wl)
+        return run_reference(args, wls[args.workload])
 
     import torch
     import torch.distributed as dist
@@ -408,6 +426,10 @@ def main():
     if world > 1:
         dist.init_process_group("nccl")
     stream = torch.cuda.current_stream()
+    # weak scaling: each rank runs its own shard (a distinct group of
+    # sequences) of a global batch world times the workload's
+    wls = {k: synth.shard(w, rank, world) for k, w in wls.items()}
+    wl = wls[args.workload]
 
     head = measure(wl, args, m3, torch, dist, world, local, stream, headline=True)
     others = []

@@ -118,6 +118,12 @@ class Workload:
     len_hi: int = 0
     seed: int = 0
     cu_seqlens: np.ndarray | None = field(default=None, repr=False)
+    # shard of a global problem: this shard's `batch` sequences (varlen:
+    # `nseq` sequences) are number shard_index*batch.. of a global batch of
+    # shards*batch
+    shard_index: int = 0
+    shards: int = 1
+    tok_offset: int = 0  # varlen: first global token of this shard
 
     @property
     def units(self) -> int:
@@ -149,6 +155,26 @@ def workloads() -> dict:
     return w
 
 
+def shard(wl: Workload, rank: int, world: int) -> Workload:
+    """Rank `rank`'s part of the global problem made of `world` copies of
+    `wl`'s batch: the global batch is world*batch sequences (varlen:
+    world*nseq packed sequences, lengths drawn for all of them), and this
+    rank holds a contiguous group of them.  Per-head weights (A, D) are the
+    same on every rank.  Concatenating the shards' tensors over ranks gives
+    exactly the global problem's tensors."""
+    if not (0 <= rank < world):
+        raise ValueError("rank out of range")
+    out = scaled(wl, shard_index=rank, shards=world)
+    if wl.kind == "varlen":
+        lens = lengths(wl.nseq * world, wl.len_lo, wl.len_hi, seed=wl.seed)
+        glob = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        mine = lens[rank * wl.nseq:(rank + 1) * wl.nseq]
+        out.cu_seqlens = np.concatenate([[0], np.cumsum(mine)]).astype(np.int32)
+        out.seqlen = int(out.cu_seqlens[-1])
+        out.tok_offset = int(glob[rank * wl.nseq])
+    return out
+
+
 def scaled(wl: Workload, **kw) -> Workload:
     """A copy of ``wl`` with some fields replaced (smaller parity-test sizes)."""
     d = dict(wl.__dict__)
@@ -170,21 +196,34 @@ def prefill_inputs(wl: Workload) -> dict:
     b, L, H, P, N, R = wl.batch, wl.seqlen, wl.nheads, wl.headdim, wl.dstate, wl.rank
     dt_ = wl.dtype
     s = wl.seed
+    # first token (over b*L) and first unit of this shard in the global problem
+    t0 = wl.tok_offset if wl.kind == "varlen" else wl.shard_index * b * L
+    u0 = wl.shard_index * (wl.nseq if wl.kind == "varlen" else b) * H
+
+    def tok(shape, stream, kind, p0, p1, row_len=0):
+        per_tok = int(np.prod(shape[2:]))
+        return fill(shape, stream, kind, p0, p1, dt_, s, offset=t0 * per_tok, row_len=row_len)
+
+    def unit(shape, stream, kind, p0, p1, dtype, row_len=0):
+        per_unit = int(np.prod(shape[2:]))
+        return fill(shape, stream, kind, p0, p1, dtype, s, offset=u0 * per_unit, row_len=row_len)
+
     d = {
-        "x": fill((b, L, H, R, P), S_X, K_NORMAL, 0.0, 1.0, dt_, s),
-        "B": fill((b, L, H, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, s, row_len=N),
-        "C": fill((b, L, H, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, s, row_len=N),
-        "dt": fill((b, L, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0, dt_, s),
-        "lam": fill((b, L, H), S_LAM, K_SIGMOID, 0.0, 0.0, dt_, s),
-        "theta": fill((b, L, H, N // 2), S_THETA, K_UNIFORM, 0.0, np.pi, dt_, s),
+        "x": tok((b, L, H, R, P), S_X, K_NORMAL, 0.0, 1.0),
+        "B": tok((b, L, H, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "C": tok((b, L, H, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "dt": tok((b, L, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
+        "lam": tok((b, L, H), S_LAM, K_SIGMOID, 0.0, 0.0),
+        "theta": tok((b, L, H, N // 2), S_THETA, K_UNIFORM, 0.0, np.pi),
         "A": fill((H,), S_A, K_NEG_EXP, 0.0, 0.5, "f32", s),
         "D": fill((H,), S_D, K_NORMAL, 0.0, 1.0, "f32", s),
     }
+    nseq = wl.nseq if wl.kind == "varlen" else b
     if wl.h0_std > 0:
-        d["h0"] = fill((b, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32", s)
+        d["h0"] = unit((nseq, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32")
     if wl.carry:
-        d["prev_B"] = fill((b, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, s, row_len=N)
-        d["prev_x"] = fill((b, H, R, P), S_PREVX, K_NORMAL, 0.0, 1.0, dt_, s)
+        d["prev_B"] = unit((nseq, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, row_len=N)
+        d["prev_x"] = unit((nseq, H, R, P), S_PREVX, K_NORMAL, 0.0, 1.0, dt_)
     return d
 
 
@@ -203,8 +242,22 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
     s = wl.seed
 
     def step_fill(inner, stream, kind, p0, p1, row_len=0):
-        n = int(np.prod(inner))
-        return fill((T,) + inner, stream, kind, p0, p1, dt_, s, offset=first_step * n, row_len=row_len)
+        n = int(np.prod(inner))  # this shard's elements per step
+        if wl.shards == 1:
+            return fill((T,) + inner, stream, kind, p0, p1, dt_, s, offset=first_step * n, row_len=row_len)
+        # step t of the global problem is elements t*n*world.. of the stream; this shard's slice is
+        # at rank*n inside it
+        out = np.empty((T,) + inner, dtype=np.uint16 if dt_ == "bf16" else np.float32)
+        for t in range(T):
+            out[t] = fill(inner, stream, kind, p0, p1, dt_, s,
+                          offset=((first_step + t) * wl.shards + wl.shard_index) * n, row_len=row_len)
+        return out
+
+    u0 = wl.shard_index * b * H  # first unit of this shard
+
+    def unit(shape, stream, kind, p0, p1, dtype, row_len=0):
+        per_unit = int(np.prod(shape[2:]))
+        return fill(shape, stream, kind, p0, p1, dtype, s, offset=u0 * per_unit, row_len=row_len)
 
     d = {
         "x": step_fill((b, H, R, P), S_X, K_NORMAL, 0.0, 1.0),
@@ -217,12 +270,12 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
         "D": fill((H,), S_D, K_NORMAL, 0.0, 1.0, "f32", s),
     }
     if wl.h0_std > 0:
-        d["h0"] = fill((b, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32", s)
+        d["h0"] = unit((b, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32")
     else:
         d["h0"] = np.zeros((b, H, N // 2, P, 2), np.float32)
     if wl.carry:
-        d["prev_B"] = fill((b, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, s, row_len=N)
-        d["prev_x"] = fill((b, H, R, P), S_PREVX, K_NORMAL, 0.0, 1.0, dt_, s)
+        d["prev_B"] = unit((b, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, row_len=N)
+        d["prev_x"] = unit((b, H, R, P), S_PREVX, K_NORMAL, 0.0, 1.0, dt_)
     else:
         z = np.uint16 if dt_ == "bf16" else np.float32
         d["prev_B"] = np.zeros((b, H, R, N), z)
