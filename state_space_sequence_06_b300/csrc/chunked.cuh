@@ -272,40 +272,45 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const int k = pt % K2, g = pt / K2;  // rotation: pair k for the tokens of group g
     if (pt < K2) sPhi[pt] = 0.f;
-    // dt and lam of token pt of a chunk (token Q: the next chunk's first), loaded one chunk ahead
-    auto load_scalars = [&](int c, float& d, float& l) {
-      d = 0.f;
-      l = 0.f;
+    // dt and lam of token pt of a chunk (token Q: the next chunk's first),
+    // loaded one chunk ahead as raw bf16 bits: converting them only where
+    // they are used keeps the load latency behind a whole chunk of work
+    const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(p.dt);
+    const unsigned short* lam_bits = reinterpret_cast<const unsigned short*>(p.lam);
+    auto load_scalars = [&](int c, uint32_t& d, uint32_t& l) {
+      d = 0u;
+      l = 0u;
       if (pt <= Q && c < nchunks) {
         const int64_t i = (int64_t)c * Q + pt;
         if (i < ntok) {
-          d = __bfloat162float(p.dt[(tok0 + i) * H + head]);
-          l = __bfloat162float(p.lam[(tok0 + i) * H + head]);
+          d = __ldg(dt_bits + (tok0 + i) * H + head);
+          l = __ldg(lam_bits + (tok0 + i) * H + head);
         }
       }
     };
-    float d_cur, l_cur;
+    uint32_t d_cur, l_cur;
     load_scalars(0, d_cur, l_cur);
     // prologue of chunk c: scalars, angle scan, rotation of B and C, X and W X.
     // Returns false when the pipeline was aborted.
     auto prologue = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
-      float d_nxt, l_nxt;
+      uint32_t d_nxt, l_nxt;
       load_scalars(c + 1, d_nxt, l_nxt);
       bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       // scalar slot xs last served chunk c - XB: its output must be done
       if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(1, NPRO, got)) return false;
       // ---- per-token scalars and the inclusive scan of dt * A
+      const float dcur = __uint_as_float(d_cur << 16), lcur = __uint_as_float(l_cur << 16);
       if (pt <= Q) {
-        sDt[pt] = d_cur;
-        sBet[pt] = (1.f - l_cur) * d_cur;
-        if (pt < Q) sGam[xs][pt] = l_cur * d_cur;
+        sDt[pt] = dcur;
+        sBet[pt] = (1.f - lcur) * dcur;
+        if (pt < Q) sGam[xs][pt] = lcur * dcur;
       }
       // (whole warps take part in the shuffles: tokens Q..QW-1 contribute zero)
       constexpr int QW = (Q + 31) / 32 * 32;
-      float v = (pt < Q) ? d_cur * A : 0.f;
+      float v = (pt < Q) ? dcur * A : 0.f;
       if (pt < QW) {
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -411,61 +416,65 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         got = wait_or_abort(saddr(&bar_yfull[(c - 1) & 1]), (uint32_t)(((c - 1) >> 1) & 1), abort_flag);
       if (!group_and(1, NPRO, got)) return false;
       tc_fence_after();
+      // warp w covers accumulator rows 16(w%4) .. +15 (TMEM lane quarter w%4)
+      // and one half of the columns; with the 16x256b shape thread `lane`
+      // holds rows r0 = 16(w%4) + lane/4 and r0 + 8, columns 8g + 2(lane%4)
+      // + {0, 1} of each 8-column group g: all 32 lanes carry data
       const int q4 = warp & 3;
-      const int t = acc_row_of(MR, q4, lane);
-      const int it = t >= 0 ? t / R : 0;
+      const int r0 = 16 * q4 + lane / 4;
+      const int it0 = r0 / R, it1 = (r0 + 8) / R;
       // last token held by this warp's rows: column blocks past it are all masked
       const int it_warp = (16 * q4 + 15) / R;
-      const float elam_t = sELam[xs][it], lam_t = sLam[xs][it], gam_t = sGam[xs][it];
+      const float elam0 = sELam[xs][it0], lam0 = sLam[xs][it0], gam0 = sGam[xs][it0];
+      const float elam1 = sELam[xs][it1], lam1 = sLam[xs][it1], gam1 = sGam[xs][it1];
       const bool factor = lam_end > -60.f;  // e^{Lam_t} and e^{-Lam_j} both stay normal floats
       constexpr int CPH = MR / 2;           // columns per warp half
       const int cbeg = (warp >> 2) * CPH;
-      float sv[CPH], bw[CPH / R];
-#pragma unroll
-      for (int q = 0; q < CPH / R; q += 4) {
-        const float4 w4 = *reinterpret_cast<const float4*>(&sBw[xs][cbeg / R + q]);
-        bw[q] = w4.x;
-        bw[q + 1] = w4.y;
-        bw[q + 2] = w4.z;
-        bw[q + 3] = w4.w;
-      }
+      const int cl = 2 * (lane % 4);        // this thread's column pair inside each 8-column group
+      float sv[CPH / 2];                    // [group g][4]: (r0, c), (r0, c+1), (r0+8, c), (r0+8, c+1)
 #pragma unroll
       for (int cb = 0; cb < CPH; cb += 16) {
-        float tmp[16];
+        float tmp[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) tmp[i] = 0.f;
-        if ((cbeg + cb) / R <= it_warp) tmem_ld16(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, tmp);
+        for (int i = 0; i < 8; ++i) tmp[i] = 0.f;
+        if ((cbeg + cb) / R <= it_warp) tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, tmp);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sv[cb + i] = tmp[i];
+        for (int i = 0; i < 8; ++i) sv[cb / 2 + i] = tmp[i];
       }
       tmem_ld_wait();
-      if (t >= 0) {
 #pragma unroll
-        for (int cb = 0; cb < CPH; cb += 8) {
-          uint32_t hv[4], lv[4];
-          if ((cbeg + cb) / R > it) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) hv[q] = lv[q] = 0u;
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float e[2];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int j = cbeg + cb + 2 * q + u, jt = j / R;
-                const float sij = sv[cb + 2 * q + u];
-                const float off = factor ? sij * bw[(cb + 2 * q + u) / R] * elam_t
-                                         : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
-                e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
-              }
-              split_half2(e[0], e[1], hv[q], lv[q]);
-            }
-          }
-          const int j = cbeg + cb;
-          const uint32_t o = (j / 64) * (MR * 128) + sw128_offset(t, j % 64);
-          *reinterpret_cast<uint4*>(St + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          *reinterpret_cast<uint4*>(Stlo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      for (int g8 = 0; g8 < CPH / 8; ++g8) {
+        const int j = cbeg + 8 * g8 + cl;  // first of this thread's two columns
+        float bw2[2];
+        if (R == 1) {
+          const float2 w2 = *reinterpret_cast<const float2*>(&sBw[xs][j]);
+          bw2[0] = w2.x;
+          bw2[1] = w2.y;
+        } else {
+          bw2[0] = sBw[xs][j / R];
+          bw2[1] = sBw[xs][(j + 1) / R];
         }
+        uint32_t hv[2], lv[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int it = rr ? it1 : it0;
+          const float elam_t = rr ? elam1 : elam0, lam_t = rr ? lam1 : lam0, gam_t = rr ? gam1 : gam0;
+          float e[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int jt = (j + u) / R;
+            const float sij = sv[4 * g8 + 2 * rr + u];
+            const float off = factor ? sij * bw2[u] * elam_t : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
+            e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
+          }
+          split_half2(e[0], e[1], hv[rr], lv[rr]);
+        }
+        const uint32_t o0 = (j / 64) * (MR * 128) + sw128_offset(r0, j % 64);
+        const uint32_t o1 = (j / 64) * (MR * 128) + sw128_offset(r0 + 8, j % 64);
+        *reinterpret_cast<uint32_t*>(St + o0) = hv[0];
+        *reinterpret_cast<uint32_t*>(Stlo + o0) = lv[0];
+        *reinterpret_cast<uint32_t*>(St + o1) = hv[1];
+        *reinterpret_cast<uint32_t*>(Stlo + o1) = lv[1];
       }
       tc_fence_before();
       fence_async_smem();

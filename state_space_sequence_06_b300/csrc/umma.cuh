@@ -99,6 +99,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 lanes x 256 bits, twice along the columns (16 f32 columns from taddr):
+// thread t gets, for column group j = 0, 1 (8 columns each), the elements
+// (lane t/4, columns 8j + 2(t%4) + {0,1}) in v[4j], v[4j+1] and (lane
+// t/4 + 8, the same columns) in v[4j+2], v[4j+3].  All 32 threads carry data
+// for a 16-row (M = 64) accumulator slice, unlike the 32x32b shape.
+__device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {

@@ -19,7 +19,8 @@ class ProbeArgs(ctypes.Structure):
                 ("err", ctypes.c_void_p), ("a_bytes", ctypes.c_int), ("b_bytes", ctypes.c_int),
                 ("a_lbo", ctypes.c_uint32), ("a_sbo", ctypes.c_uint32), ("b_lbo", ctypes.c_uint32),
                 ("b_sbo", ctypes.c_uint32), ("a_kstep", ctypes.c_uint32), ("b_kstep", ctypes.c_uint32),
-                ("nk", ctypes.c_int), ("idesc", ctypes.c_uint32), ("ncols", ctypes.c_int)]
+                ("nk", ctypes.c_int), ("idesc", ctypes.c_uint32), ("ncols", ctypes.c_int),
+                ("out2", ctypes.c_void_p)]
 
 
 @pytest.fixture(scope="module")
@@ -60,7 +61,7 @@ def idesc(M, N, a_mn, b_mn):
     return (1 << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24)
 
 
-def run(lib, A, B, a_off, b_off, a_lbo, a_sbo, b_lbo, b_sbo, a_step, b_step, M, N, a_mn, b_mn):
+def run(lib, A, B, a_off, b_off, a_lbo, a_sbo, b_lbo, b_sbo, a_step, b_step, M, N, a_mn, b_mn, out2=None):
     K = A.shape[1]
     a_img = np.zeros(65536, np.uint8)
     b_img = np.zeros(65536, np.uint8)
@@ -78,7 +79,7 @@ def run(lib, A, B, a_off, b_off, a_lbo, a_sbo, b_lbo, b_sbo, a_step, b_step, M, 
     assert all(steps_a[i] - steps_a[0] == i * (steps_a[1] - steps_a[0]) for i in range(nk)) or nk == 1
     args = ProbeArgs(ta.data_ptr(), tb.data_ptr(), out.data_ptr(), err.data_ptr(), 65536, 65536,
                      a_lbo, a_sbo, b_lbo, b_sbo, (steps_a[1] if nk > 1 else 0), (steps_b[1] if nk > 1 else 0),
-                     nk, idesc(M, N, a_mn, b_mn), N)
+                     nk, idesc(M, N, a_mn, b_mn), N, 0 if out2 is None else out2.data_ptr())
     assert lib.umma_probe_run(ctypes.byref(args)) == 0
     assert err.item() == 0, "mbarrier wait timed out"
     return out.cpu().numpy()
@@ -136,3 +137,26 @@ def test_a_mn_major(probe, M, K):
     else:
         rows = [(r // 16) * 32 + r % 16 for r in range(64)]
         np.testing.assert_allclose(got[rows], ref, rtol=0, atol=1e-5)
+
+
+def test_ld_16x256b_layout(probe):
+    """The 16x256b TMEM load shape: thread t of warp w reads, for each
+    8-column group j, lane 32w + t/4 (+ 8 for the second pair) and columns
+    8j + 2(t%4) + {0, 1}; checked against the 32x32b dump of the same
+    accumulator (M = 128, every lane distinct)."""
+    N, K = 64, 64
+    A, B = rand((128, K), 9), rand((N, K), 10)
+    ao, _, astep = kmajor_image(128, K)
+    bo, _, bstep = kmajor_image(N, K)
+    out2 = torch.full((4, N // 16, 32, 8), float("nan"), device="cuda")
+    got = run(probe, A, B, ao, bo, 16, 1024, 16, 1024, astep, bstep, 128, N, 0, 0, out2=out2)
+    np.testing.assert_allclose(got, A @ B.T, rtol=0, atol=1e-5)
+    o2 = out2.cpu().numpy()
+    for w in range(4):
+        for cb in range(N // 16):
+            for t in range(32):
+                for i in range(8):
+                    j, q = divmod(i, 4)
+                    lane = 32 * w + t // 4 + 8 * (q // 2)
+                    col = 16 * cb + 8 * j + 2 * (t % 4) + (q % 2)
+                    assert o2[w, cb, t, i] == got[lane, col], (w, cb, t, i)

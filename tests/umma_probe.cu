@@ -21,6 +21,8 @@ struct ProbeArgs {
   int nk;
   uint32_t idesc;
   int ncols;  // accumulator columns to dump (multiple of 16, <= 256)
+  float* out2;  // optional: the same columns read with the 16x256b shape,
+                // [warp][ncols / 16][thread][8] (lanes 32*warp .. 32*warp + 15)
 };
 
 constexpr int kTileBytes = 65536;
@@ -69,6 +71,15 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(const ProbeArgs p) {
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 16; ++i) p.out[(32 * warp + lane) * p.ncols + c + i] = v[i];
+  }
+  if (p.out2) {
+    for (int c = 0; c < p.ncols; c += 16) {
+      float v[8];
+      tmem_ld16x256b_x2(tmem + ((uint32_t)(32 * warp) << 16) + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p.out2[((warp * (p.ncols / 16) + c / 16) * 32 + lane) * 8 + i] = v[i];
+    }
   }
   tc_fence_before();
   __syncthreads();
