@@ -156,18 +156,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Bounded wait.  Gives up (and makes every role of this CTA give up) when
 // the phase has not completed within kWaitLimitNs, or as soon as another
-// role of this CTA or any other CTA has recorded a failure, so a stalled
-// pipeline ends the launch in well under a second with M3_ERR_TIMEOUT.
-// abort_flag[0] is this CTA's flag, abort_flag[1] the value the device
-// status word held when the CTA started (a failure of an earlier launch
-// must not stop this one).
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (umma::mbar_try_wait(bar, parity)) return true;
+// role of this CTA has recorded a failure, so a stalled pipeline ends each
+// CTA within a fraction of a second with M3_ERR_TIMEOUT.  abort_flag[0] is
+// this CTA's flag.  Waiting threads read nothing outside their own CTA: a
+// poll of a global word by every waiting warp of every CTA costs memory
+// requests the pipeline needs.
+//
+// Only the first poll is inlined at each call site; the loop is one shared
+// out-of-line copy.  The kernel's roles run different code at the same time
+// on one SM, and instruction fetch is a shared resource: every copy of code
+// that is executed each chunk costs instruction-cache capacity.
+__device__ __noinline__ bool wait_or_abort_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kMaxPolls; ++i) {
     if (umma::mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
-      if (abort_flag[0] || *(volatile int*)&g_status != abort_flag[1]) {
+      if (abort_flag[0]) {
         abort_flag[0] = 1;
         return false;
       }
@@ -177,6 +181,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   abort_flag[0] = 1;
   atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
   return false;
+}
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (umma::mbar_try_wait(bar, parity)) return true;
+  return wait_or_abort_slow(bar, parity, abort_flag);
 }
 
 template <int N, int R, int Q>
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB];
   __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_gfull;
   __shared__ uint32_t tmem_base_s;
-  __shared__ int s_abort[2];  // this CTA's abort flag; the status word at start
+  __shared__ int s_abort[1];  // this CTA's abort flag
   // per-chunk scalars, one set per X slot (chunk c uses slot c % XB)
   __shared__ float sLam[XB][Q], sELam[XB][Q], sGam[XB][Q], sWp[XB][Q], sDw[XB][Q], sLamEnd[XB];
   __shared__ __align__(16) float sBw[XB][Q];
@@ -240,7 +248,6 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
 
   if (tid == 0) {
     s_abort[0] = 0;
-    s_abort[1] = *(volatile int*)&g_status;
     for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_full[s]), 1);
       mbar_init(saddr(&bar_opready[s]), 1);
@@ -431,50 +438,49 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       constexpr int CPH = MR / 2;           // columns per warp half
       const int cbeg = (warp >> 2) * CPH;
       const int cl = 2 * (lane % 4);        // this thread's column pair inside each 8-column group
-      float sv[CPH / 2];                    // [group g][4]: (r0, c), (r0, c+1), (r0+8, c), (r0+8, c+1)
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < CPH; cb += 16) {
-        float tmp[8];
+        float sv[8];  // [group gg][4]: (r0, c), (r0, c+1), (r0+8, c), (r0+8, c+1)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) tmp[i] = 0.f;
-        if ((cbeg + cb) / R <= it_warp) tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, tmp);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sv[cb / 2 + i] = tmp[i];
-      }
-      tmem_ld_wait();
-#pragma unroll
-      for (int g8 = 0; g8 < CPH / 8; ++g8) {
-        const int j = cbeg + 8 * g8 + cl;  // first of this thread's two columns
-        float bw2[2];
-        if (R == 1) {
-          const float2 w2 = *reinterpret_cast<const float2*>(&sBw[xs][j]);
-          bw2[0] = w2.x;
-          bw2[1] = w2.y;
-        } else {
-          bw2[0] = sBw[xs][j / R];
-          bw2[1] = sBw[xs][(j + 1) / R];
+        for (int i = 0; i < 8; ++i) sv[i] = 0.f;
+        if ((cbeg + cb) / R <= it_warp) {
+          tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, sv);
+          tmem_ld_wait();
         }
-        uint32_t hv[2], lv[2];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int it = rr ? it1 : it0;
-          const float elam_t = rr ? elam1 : elam0, lam_t = rr ? lam1 : lam0, gam_t = rr ? gam1 : gam0;
-          float e[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int jt = (j + u) / R;
-            const float sij = sv[4 * g8 + 2 * rr + u];
-            const float off = factor ? sij * bw2[u] * elam_t : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
-            e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
+        for (int gg = 0; gg < 2; ++gg) {
+          const int j = cbeg + cb + 8 * gg + cl;  // first of this thread's two columns
+          float bw2[2];
+          if (R == 1) {
+            const float2 w2 = *reinterpret_cast<const float2*>(&sBw[xs][j]);
+            bw2[0] = w2.x;
+            bw2[1] = w2.y;
+          } else {
+            bw2[0] = sBw[xs][j / R];
+            bw2[1] = sBw[xs][(j + 1) / R];
           }
-          split_half2(e[0], e[1], hv[rr], lv[rr]);
+          uint32_t hv[2], lv[2];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int it = rr ? it1 : it0;
+            const float elam_t = rr ? elam1 : elam0, lam_t = rr ? lam1 : lam0, gam_t = rr ? gam1 : gam0;
+            float e[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int jt = (j + u) / R;
+              const float sij = sv[4 * gg + 2 * rr + u];
+              const float off = factor ? sij * bw2[u] * elam_t : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
+              e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
+            }
+            split_half2(e[0], e[1], hv[rr], lv[rr]);
+          }
+          const uint32_t o0 = (j / 64) * (MR * 128) + sw128_offset(r0, j % 64);
+          const uint32_t o1 = (j / 64) * (MR * 128) + sw128_offset(r0 + 8, j % 64);
+          *reinterpret_cast<uint32_t*>(St + o0) = hv[0];
+          *reinterpret_cast<uint32_t*>(Stlo + o0) = lv[0];
+          *reinterpret_cast<uint32_t*>(St + o1) = hv[1];
+          *reinterpret_cast<uint32_t*>(Stlo + o1) = lv[1];
         }
-        const uint32_t o0 = (j / 64) * (MR * 128) + sw128_offset(r0, j % 64);
-        const uint32_t o1 = (j / 64) * (MR * 128) + sw128_offset(r0 + 8, j % 64);
-        *reinterpret_cast<uint32_t*>(St + o0) = hv[0];
-        *reinterpret_cast<uint32_t*>(Stlo + o0) = lv[0];
-        *reinterpret_cast<uint32_t*>(St + o1) = hv[1];
-        *reinterpret_cast<uint32_t*>(Stlo + o1) = lv[1];
       }
       tc_fence_before();
       fence_async_smem();
@@ -535,7 +541,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         uint8_t* Xs = stg + Cfg::OFF_X;
         uint8_t* WXlo = stg + Cfg::OFF_WXLO;
         uint8_t* Xb = xbuf(xs);
-#pragma unroll
+#pragma unroll 1
         for (int idx = tt; idx < MR * (P / 8); idx += NSTA) {
           const int row = idx / (P / 8), c8 = idx % (P / 8);
           const uint32_t o = sw128_offset(row, c8 * 8);
@@ -562,30 +568,36 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       tc_fence_after();
       // rotating frame: R = G' is the f16 operand of MMA 3, then G' <- e^{Lam_end} G'
       const float elam_end = __expf(sLamEnd[xs]);
-      float v[P];
+#pragma unroll 1
+      for (int hc = 0; hc < P; hc += 32) {  // two halves of 32 columns
+        float v[32];
+        {
+          float t0[16], t1[16];
+          tmem_ld16(tmem + lane_base + Cfg::COL_G + hc, t0);
+          tmem_ld16(tmem + lane_base + Cfg::COL_G + hc + 16, t1);
+          tmem_ld_wait();
 #pragma unroll
-      for (int cb = 0; cb < P; cb += 16) {
-        float tmp[16];
-        tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, tmp);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[cb + i] = tmp[i];
-      }
-      tmem_ld_wait();
-      if (g_row >= 0) {
-#pragma unroll
-        for (int pc = 0; pc < P; pc += 8) {
-          const uint32_t o = sw128_offset(g_row, pc);
-          *reinterpret_cast<uint4*>(Rt + o) =
-              make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
-                         pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
+          for (int i = 0; i < 16; ++i) {
+            v[i] = t0[i];
+            v[16 + i] = t1[i];
+          }
         }
-      }
+        if (g_row >= 0) {
 #pragma unroll
-      for (int cb = 0; cb < P; cb += 16) {
-        float tmp[16];
+          for (int pc = 0; pc < 32; pc += 8) {
+            const uint32_t o = sw128_offset(g_row, hc + pc);
+            *reinterpret_cast<uint4*>(Rt + o) =
+                make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
+                           pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
+          }
+        }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) tmp[i] = v[cb + i] * elam_end;
-        tmem_st16(tmem + lane_base + Cfg::COL_G + cb, tmp);
+        for (int q = 0; q < 2; ++q) {
+          float tmp[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) tmp[i] = v[16 * q + i] * elam_end;
+          tmem_st16(tmem + lane_base + Cfg::COL_G + hc + 16 * q, tmp);
+        }
       }
       tmem_st_wait();
       fence_async_smem();
@@ -603,42 +615,46 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         return false;
       tc_fence_after();
       const uint8_t* Xb = xbuf(xs);
-      const int t = acc_row_of(MR, q4, lane);
-      const int it = t >= 0 ? t / R : 0, rk = t >= 0 ? t % R : 0;
-      const bool valid = t >= 0 && it < nvalid;
-      const float el = sELam[xs][it];
-      float* yrow = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
+      // 16x256b shape: thread `lane` holds rows r0 = 16(w%4) + lane/4 and
+      // r0 + 8, columns 8g + 2(lane%4) + {0, 1} of each 8-column group g, so
+      // every store of a warp fills eight whole 32-byte sectors of y
+      const int r0 = 16 * q4 + lane / 4, cl = 2 * (lane % 4);
+      bool valid[2];
+      float el[2];
+      float* yrow[2];
 #pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int t = r0 + 8 * rr, it = t / R, rk = t % R;
+        valid[rr] = it < nvalid;
+        el[rr] = sELam[xs][it];
+        yrow[rr] = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
+      }
+#pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        float a[32], b[32];
+        float a[16], b[16];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          float ta[16], tb[16];
-          tmem_ld16(tmem + lane_base + Cfg::COL_Y + s * P + 32 * half + 16 * q, ta);
-          tmem_ld16(tmem + lane_base + Cfg::COL_YI + s * P + 32 * half + 16 * q, tb);
+          float ta[8], tb[8];
+          tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_Y + s * P + 32 * half + 16 * q, ta);
+          tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_YI + s * P + 32 * half + 16 * q, tb);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            a[16 * q + i] = ta[i];
-            b[16 * q + i] = tb[i];
+          for (int i = 0; i < 8; ++i) {
+            a[8 * q + i] = ta[i];
+            b[8 * q + i] = tb[i];
           }
         }
         tmem_ld_wait();
-        if (valid) {
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            const int col = 32 * half + 8 * c8;
-            const uint4 xv = *reinterpret_cast<const uint4*>(Xb + sw128_offset(t, col));
-            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-            float o[8];
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int col = 32 * half + 8 * g8 + cl;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xs[q]));
-              const int i0 = 8 * c8 + 2 * q;
-              o[2 * q] = fmaf(Dh, f.x, fmaf(el, b[i0], a[i0]));
-              o[2 * q + 1] = fmaf(Dh, f.y, fmaf(el, b[i0 + 1], a[i0 + 1]));
-            }
-            *reinterpret_cast<float4*>(yrow + col) = make_float4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<float4*>(yrow + col + 4) = make_float4(o[4], o[5], o[6], o[7]);
+          for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t xv = *reinterpret_cast<const uint32_t*>(Xb + sw128_offset(r0 + 8 * rr, col));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xv));
+            const int i0 = 4 * g8 + 2 * rr;
+            const float o0 = fmaf(Dh, f.x, fmaf(el[rr], b[i0], a[i0]));
+            const float o1 = fmaf(Dh, f.y, fmaf(el[rr], b[i0 + 1], a[i0 + 1]));
+            if (valid[rr]) *reinterpret_cast<float2*>(yrow[rr] + col) = make_float2(o0, o1);
           }
         }
       }
@@ -705,7 +721,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         // S = C B^T = Chi Bhi^T + Chi Blo^T + Clo Bhi^T   (M = MR, N = MR, K = N)
         constexpr uint32_t idesc = idesc_f16_f32(MR, MR, 0, 0);
         const uint32_t d = tmem + Cfg::COL_S + s * MR;
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < N / 16; ++ks) {
           mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, ks > 0);
           mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, MR * 128), idesc, 1);
@@ -726,7 +742,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         // Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16)
         const uint32_t Xb = saddr(xbuf(c % XB));
         constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < MR / 16; ++ks) {
           mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(St), ks, MR * 128), mnmaj(Xb, ks, MR * 128), idesc, ks > 0);
           mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(Stlo), ks, MR * 128), mnmaj(Xb, ks, MR * 128), idesc, 1);
@@ -747,7 +763,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         tc_fence_after();
         {  // state += B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
           constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < MR / 16; ++ks) {
             mma_f16(tmem + Cfg::COL_G, mnmaj(Bt, ks, MR * 128), mnmaj(WXt, ks, MR * 128), idesc, 1);
             mma_f16(tmem + Cfg::COL_G, mnmaj(Bt, ks, MR * 128), mnmaj(WXlo, ks, MR * 128), idesc, 1);
@@ -756,7 +772,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         }
         {  // Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
           constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < N / 16; ++ks) {
             mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Ct, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, ks > 0);
             mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
