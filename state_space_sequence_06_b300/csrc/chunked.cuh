@@ -74,10 +74,11 @@ struct ChunkCfg {
   static constexpr int MR = Q * R;  // rows of S and Y: (token, rank)
   static_assert(MR == 64, "Q*R must be 64 (S and the outputs are double-buffered in TMEM)");
   static_assert(N == 64 || N == 128, "N must be 64 or 128");
-  // warp roles: 8 prologue warps, 4 state/output warps, then one warp each
-  // for the intra-chunk MMAs (1 and 2), the TMA loads and the state-chain
-  // MMAs (4 and 3)
-  static constexpr int NPRO = 256, NSTA = 128, NT = NPRO + NSTA + 96;
+  // warp roles: prologue warps (16 for SISO, 8 for MIMO, whose per-thread
+  // state is larger), 4 state/output warps, then one warp each for the
+  // intra-chunk MMAs (1 and 2), the TMA loads and the state-chain MMAs (4
+  // and 3).  The prologue's work is latency-bound: more warps hide more of it.
+  static constexpr int NPRO = R == 1 ? 512 : 256, NSTA = 128, NT = NPRO + NSTA + 96;
   static constexpr int W_STA = NPRO / 32, W_MMA = W_STA + NSTA / 32, W_TMA = W_MMA + 1, W_MMA2 = W_TMA + 1;
   // rotation work split: consecutive threads take consecutive pairs (so
   // shared-memory rows are read without bank conflicts), G token groups
@@ -90,7 +91,10 @@ struct ChunkCfg {
   static constexpr int CT_BYTES = MR * N * 2;  // C, B tiles: [N/64 blocks][MR rows][128 B]
   static constexpr int XT_BYTES = MR * P * 2;  // X, WX tiles: [MR rows][128 B]
   static constexpr int TH_BYTES = Q * K2 * 2;  // theta [Q][K2] bf16 (unswizzled)
-  static constexpr int OFF_C = 0, OFF_B = CT_BYTES, OFF_CLO = 2 * CT_BYTES, OFF_BLO = 3 * CT_BYTES;
+  // B hi and lo are interleaved per 64-column block (block kb: hi at
+  // OFF_B + kb * BB, lo MR rows after it)
+  static constexpr int OFF_C = 0, OFF_CLO = CT_BYTES, OFF_B = 2 * CT_BYTES, OFF_BLO = OFF_B + MR * 128;
+  static constexpr int BB = 2 * MR * 128;  // bytes between B blocks
   static constexpr int OFF_X = 4 * CT_BYTES;  // x (bf16), then (W X) hi
   static constexpr int OFF_TH = OFF_X + XT_BYTES;
   static constexpr bool WXLO_IN_TH = TH_BYTES >= XT_BYTES;
@@ -108,10 +112,11 @@ struct ChunkCfg {
   static constexpr int OFF_RT = OFF_STLO + ST_BYTES;
   static constexpr int SMEM = OFF_RT + RT_BYTES + 1024;  // + alignment slack
   static_assert(SMEM + STATIC_EST <= 232448, "shared memory of one CTA");
-  // TMEM columns (f32): S[2], Y[2], Yi[2], state
+  // TMEM columns (f32): S[2], Y[2], Yi[2], state, chunk-local state
   static constexpr int COL_S = 0, COL_Y = 2 * MR, COL_YI = 2 * MR + 2 * P, COL_G = 2 * MR + 4 * P;
+  static constexpr int COL_SC = COL_G + P;  // the chunk-local state B^T (W X) of MMA 4
   static constexpr int TMEM_COLS = 512;
-  static_assert(COL_G + P <= TMEM_COLS, "TMEM columns");
+  static_assert(COL_SC + P <= TMEM_COLS, "TMEM columns");
 };
 
 // TMEM lane holding row `row` of an M-row accumulator (M = 64 uses lanes
@@ -201,13 +206,16 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
   // barriers: full (TMA landed), opready (prologue done), free (stage no longer
   // read by MMAs), xready (X of the slot's chunk converted), xfree (X slot and
   // output accumulators no longer read), sfull (MMA 1 done), yfull (MMAs 2
-  // and 3 done), spready (S' written), stready (state step done), gfull
-  // (MMAs 4 and 3 done).  A phase-parity wait is only sound when the waiter
-  // can never fall two phases behind the barrier; each pairing below is
-  // chained so that it cannot.
+  // and 3 done), spready (S' written), scfull (MMA 4 done: the chunk-local
+  // state is in TMEM), scfree (the state warps have folded it into the
+  // state), stready (R, the f16 copy of the state for MMA 3, written; once
+  // before the first chunk and once per chunk), rfree (MMA 3 done reading
+  // R).  A phase-parity wait is only sound when the waiter can never fall two
+  // phases behind the barrier; each pairing below is chained so that it
+  // cannot.
   __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB];
-  __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_gfull;
+  __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_scfull, bar_scfree, bar_rfree;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_abort[1];  // this CTA's abort flag
   // per-chunk scalars, one set per X slot (chunk c uses slot c % XB)
@@ -261,7 +269,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     }
     mbar_init(saddr(&bar_spready), 1);
     mbar_init(saddr(&bar_stready), 1);
-    mbar_init(saddr(&bar_gfull), 1);
+    mbar_init(saddr(&bar_scfull), 1);
+    mbar_init(saddr(&bar_scfree), 1);
+    mbar_init(saddr(&bar_rfree), 1);
     mbar_init_fence();
   }
   if (warp == 0) {
@@ -389,13 +399,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
           const int i = g * TPG + ii;
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            const uint32_t o = blk * (MR * 128) + sw128_offset(i * R + r, col);
-            const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + o));
+            const uint32_t rc = sw128_offset(i * R + r, col);
+            const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
+            const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
             const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
             uint32_t hi, lo;
             split_half2(cs[ii] * b.x - sn[ii] * b.y, sn[ii] * b.x + cs[ii] * b.y, hi, lo);
-            *reinterpret_cast<uint32_t*>(Bt + o) = hi;
-            *reinterpret_cast<uint32_t*>(Blo + o) = lo;
+            *reinterpret_cast<uint32_t*>(Bt + ob) = hi;
+            *reinterpret_cast<uint32_t*>(Blo + ob) = lo;
             split_half2(cs[ii] * cc.x - sn[ii] * cc.y, sn[ii] * cc.x + cs[ii] * cc.y, hi, lo);
             *reinterpret_cast<uint32_t*>(Ct + o) = hi;
             *reinterpret_cast<uint32_t*>(Clo + o) = lo;
@@ -424,7 +435,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       if (!group_and(1, NPRO, got)) return false;
       tc_fence_after();
       // warp w covers accumulator rows 16(w%4) .. +15 (TMEM lane quarter w%4)
-      // and one half of the columns; with the 16x256b shape thread `lane`
+      // and one slice of CPH columns; with the 16x256b shape thread `lane`
       // holds rows r0 = 16(w%4) + lane/4 and r0 + 8, columns 8g + 2(lane%4)
       // + {0, 1} of each 8-column group g: all 32 lanes carry data
       const int q4 = warp & 3;
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       const float elam0 = sELam[xs][it0], lam0 = sLam[xs][it0], gam0 = sGam[xs][it0];
       const float elam1 = sELam[xs][it1], lam1 = sLam[xs][it1], gam1 = sGam[xs][it1];
       const bool factor = lam_end > -60.f;  // e^{Lam_t} and e^{-Lam_j} both stay normal floats
-      constexpr int CPH = MR / 2;           // columns per warp half
+      constexpr int CPH = MR / (NPRO / 128);  // columns per warp (warps w, w+4, ... share rows)
       const int cbeg = (warp >> 2) * CPH;
       const int cl = 2 * (lane % 4);        // this thread's column pair inside each 8-column group
 #pragma unroll 1
@@ -524,16 +535,24 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
           }
         }
         tmem_st16(tmem + lane_base + Cfg::COL_G + cb, v);
+        if (g_row >= 0) {  // R = f16(G') for MMA 3 of chunk 0
+#pragma unroll
+          for (int pc = 0; pc < 16; pc += 8)
+            *reinterpret_cast<uint4*>(Rt + sw128_offset(g_row, cb + pc)) =
+                make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
+                           pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
+        }
       }
       tmem_st_wait();
+      fence_async_smem();
+      group_sync(2, NSTA);
+      if (tt == 0) mbar_arrive(saddr(&bar_stready));
     }
-    // state step of chunk c: needs its scalars (prologue) and the state after MMA 4 of chunk c-1
-    auto state_step = [&](int c) -> bool {
+    // X of chunk c to f16 (slot c % XB) and W X as hi (over x) and lo parts:
+    // needs only the prologue of chunk c
+    auto xconv = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
-      // X to f16 in slot xs (its previous chunk's MMA 2 and output are done)
-      // and W X as hi (over x) and lo parts: needs only the prologue, so it
-      // overlaps MMA 4 of the previous chunk
       bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(2, NSTA, got)) return false;
@@ -541,7 +560,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         uint8_t* Xs = stg + Cfg::OFF_X;
         uint8_t* WXlo = stg + Cfg::OFF_WXLO;
         uint8_t* Xb = xbuf(xs);
-#pragma unroll 1
+#pragma unroll 4
         for (int idx = tt; idx < MR * (P / 8); idx += NSTA) {
           const int row = idx / (P / 8), c8 = idx % (P / 8);
           const uint32_t o = sw128_offset(row, c8 * 8);
@@ -563,47 +582,43 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         group_sync(2, NSTA);
         if (tt == 0) mbar_arrive(saddr(&bar_xready[xs]));
       }
-      if (c >= 1 && !group_and(2, NSTA, wait_or_abort(saddr(&bar_gfull), (uint32_t)((c - 1) & 1), abort_flag)))
-        return false;
+      return true;
+    };
+    // state step of chunk c, in the rotating frame: G' <- e^{Lam_end} G' + S_c
+    // (S_c from MMA 4 of chunk c), then R = f16(G') for MMA 3 of chunk c + 1
+    // once MMA 3 of chunk c has read the previous R
+    auto state = [&](int c) -> bool {
+      const int xs = c % XB;
+      bool got = wait_or_abort(saddr(&bar_scfull), (uint32_t)(c & 1), abort_flag);
+      if (got) got = wait_or_abort(saddr(&bar_rfree), (uint32_t)(c & 1), abort_flag);
+      if (!group_and(2, NSTA, got)) return false;
       tc_fence_after();
-      // rotating frame: R = G' is the f16 operand of MMA 3, then G' <- e^{Lam_end} G'
       const float elam_end = __expf(sLamEnd[xs]);
 #pragma unroll 1
-      for (int hc = 0; hc < P; hc += 32) {  // two halves of 32 columns
-        float v[32];
-        {
-          float t0[16], t1[16];
-          tmem_ld16(tmem + lane_base + Cfg::COL_G + hc, t0);
-          tmem_ld16(tmem + lane_base + Cfg::COL_G + hc + 16, t1);
-          tmem_ld_wait();
+      for (int hc = 0; hc < P; hc += 16) {
+        float g[16], sc[16];
+        tmem_ld16(tmem + lane_base + Cfg::COL_G + hc, g);
+        tmem_ld16(tmem + lane_base + Cfg::COL_SC + hc, sc);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            v[i] = t0[i];
-            v[16 + i] = t1[i];
-          }
-        }
+        for (int i = 0; i < 16; ++i) g[i] = fmaf(elam_end, g[i], sc[i]);
+        tmem_st16(tmem + lane_base + Cfg::COL_G + hc, g);
         if (g_row >= 0) {
 #pragma unroll
-          for (int pc = 0; pc < 32; pc += 8) {
-            const uint32_t o = sw128_offset(g_row, hc + pc);
-            *reinterpret_cast<uint4*>(Rt + o) =
-                make_uint4(pack_half2(v[pc], v[pc + 1]), pack_half2(v[pc + 2], v[pc + 3]),
-                           pack_half2(v[pc + 4], v[pc + 5]), pack_half2(v[pc + 6], v[pc + 7]));
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float tmp[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) tmp[i] = v[16 * q + i] * elam_end;
-          tmem_st16(tmem + lane_base + Cfg::COL_G + hc + 16 * q, tmp);
+          for (int pc = 0; pc < 16; pc += 8)
+            *reinterpret_cast<uint4*>(Rt + sw128_offset(g_row, hc + pc)) =
+                make_uint4(pack_half2(g[pc], g[pc + 1]), pack_half2(g[pc + 2], g[pc + 3]),
+                           pack_half2(g[pc + 4], g[pc + 5]), pack_half2(g[pc + 6], g[pc + 7]));
         }
       }
       tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       group_sync(2, NSTA);
-      if (tt == 0) mbar_arrive(saddr(&bar_stready));
+      if (tt == 0) {
+        mbar_arrive(saddr(&bar_stready));
+        mbar_arrive(saddr(&bar_scfree));
+      }
       return true;
     };
     // output of chunk c: y = Y + e^{Lam_t} Yi + D x, needs MMAs 2 and 3 of chunk c
@@ -663,15 +678,24 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       if (tt == 0) mbar_arrive(saddr(&bar_xfree[xs]));
       return true;
     };
-    // the state step runs one chunk ahead of the output
-    bool alive = state_step(0);
+    // order: X of chunk c + 1 as soon as its prologue is done, the output of
+    // chunk c (after its MMAs 2 and 3), then the state step of chunk c + 1,
+    // whose R the next MMA 3 needs long before its stage is released
+    bool alive = xconv(0) && state(0);
     for (int c = 0; c < nchunks && alive; ++c) {
-      if (c + 1 < nchunks && !state_step(c + 1)) break;
-      alive = output(c);
+      if (c + 1 < nchunks && !xconv(c + 1)) {
+        alive = false;
+        break;
+      }
+      if (!output(c)) {
+        alive = false;
+        break;
+      }
+      if (c + 1 < nchunks) alive = state(c + 1);
     }
-    // ---- final state (h of the last token) and carry (the last token's B and x)
-    if (group_and(2, NSTA, wait_or_abort(saddr(&bar_gfull), (uint32_t)((nchunks - 1) & 1), abort_flag))) {
-      tc_fence_after();
+    // ---- final state (h of the last token) and carry (the last token's B and x);
+    // `alive` is the same in every state warp (each step ends in a group vote)
+    if (alive) {
       if (p.h) {  // h = e^{i Phi_end} G' (pairs of rows are (re, im) in adjacent lanes)
         float cs = 1.f, sn = 0.f;
         if (g_row >= 0) sincosf(sPhi[g_row >> 1], &sn, &cs);
@@ -723,14 +747,15 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         const uint32_t d = tmem + Cfg::COL_S + s * MR;
 #pragma unroll 1
         for (int ks = 0; ks < N / 16; ++ks) {
-          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, ks > 0);
-          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, MR * 128), idesc, 1);
-          mma_f16(d, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, MR * 128), idesc, 1);
+          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, Cfg::BB), idesc, ks > 0);
+          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, Cfg::BB), idesc, 1);
+          mma_f16(d, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, Cfg::BB), idesc, 1);
         }
         mma_commit(saddr(&bar_sfull[s]));
         mma_commit(saddr(&bar_free[s]));
         return true;
       };
+      // intra-chunk products, MMA 1 one chunk ahead of MMA 2
       bool alive = mma1(0);
       for (int c = 0; c < nchunks && alive; ++c) {
         const int s = c & 1;
@@ -751,25 +776,21 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         mma_commit(saddr(&bar_xfree[c % XB]));
       }
     } else if (lane == 0) {
-      // state chain: MMA 4 (state update) and MMA 3 (inter-chunk output) of chunk c
+      // MMA 3 (inter-chunk output) and MMA 4 (chunk-local state) of chunk c.
+      // MMA 3 needs only this chunk's C and the R of the previous state step,
+      // so it goes first; the stage is released when MMA 4 is done.
       for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         uint8_t* stg = stage(s);
         const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
         const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
         const uint32_t WXt = saddr(stg + Cfg::OFF_X), WXlo = saddr(stg + Cfg::OFF_WXLO);
+        // C of the stage rotated (prologue); R of the state at the start of chunk c
+        // written; Yi[s] free (output of chunk c - 2 done)
+        if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
         if (!wait_or_abort(saddr(&bar_stready), (uint32_t)(c & 1), abort_flag)) break;
-        if (c >= 2 && !wait_xfree(c - 2)) break;  // Yi[s] last held the output of chunk c - 2
+        if (c >= 2 && !wait_xfree(c - 2)) break;
         tc_fence_after();
-        {  // state += B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
-          constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
-#pragma unroll 1
-          for (int ks = 0; ks < MR / 16; ++ks) {
-            mma_f16(tmem + Cfg::COL_G, mnmaj(Bt, ks, MR * 128), mnmaj(WXt, ks, MR * 128), idesc, 1);
-            mma_f16(tmem + Cfg::COL_G, mnmaj(Bt, ks, MR * 128), mnmaj(WXlo, ks, MR * 128), idesc, 1);
-            mma_f16(tmem + Cfg::COL_G, mnmaj(Blo, ks, MR * 128), mnmaj(WXt, ks, MR * 128), idesc, 1);
-          }
-        }
         {  // Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
           constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
 #pragma unroll 1
@@ -778,9 +799,23 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
             mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
           }
         }
-        // one commit covers both products: the state, R, the output accumulator and the stage
-        mma_commit(saddr(&bar_gfull));
+        mma_commit(saddr(&bar_rfree));
         mma_commit(saddr(&bar_yfull[s]));
+        // W X converted (state warps); S_{c-1} folded into the state
+        if (!wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;
+        if (c >= 1 && !wait_or_abort(saddr(&bar_scfree), (uint32_t)((c - 1) & 1), abort_flag)) break;
+        tc_fence_after();
+        {  // S_c = B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
+          constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
+#pragma unroll 1
+          for (int ks = 0; ks < MR / 16; ++ks) {
+            mma_f16(tmem + Cfg::COL_SC, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, ks > 0);
+            mma_f16(tmem + Cfg::COL_SC, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXlo, ks, MR * 128), idesc, 1);
+            mma_f16(tmem + Cfg::COL_SC, mnmaj(Blo, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, 1);
+          }
+        }
+        // each commit tracks every product issued so far by this thread
+        mma_commit(saddr(&bar_scfull));
         mma_commit(saddr(&bar_free[s]));
       }
     }
@@ -797,7 +832,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         tma_load_4d(saddr(stg + Cfg::OFF_X), &tm_x, bar, 0, 0, head, t);
 #pragma unroll
         for (int kb = 0; kb < N / 64; ++kb) {
-          tma_load_4d(saddr(stg + Cfg::OFF_B + kb * MR * 128), &tm_B, bar, 64 * kb, 0, head, t);
+          tma_load_4d(saddr(stg + Cfg::OFF_B + kb * Cfg::BB), &tm_B, bar, 64 * kb, 0, head, t);
           tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head, t);
         }
         tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);

@@ -46,7 +46,26 @@ SMALL = {
     "mimo4": dict(batch=2, seqlen=201, nheads=3, headdim=64, dstate=64, rank=4, chunk=16),
     "siso_long_dt": dict(batch=1, seqlen=517, nheads=2, headdim=64, dstate=128, rank=1, chunk=64, dt_shift=-3.0),
     "odd_shape": dict(batch=2, seqlen=45, nheads=2, headdim=32, dstate=48, rank=2, chunk=64),
+    # large dt: chunks whose summed log-decay falls below -60, where the
+    # chunked kernel takes its per-element decay path (see the coverage test)
+    "siso_strong_decay": dict(batch=1, seqlen=300, nheads=4, headdim=64, dstate=128, rank=1, chunk=64, dt_shift=1.5),
+    "mimo4_strong_decay": dict(batch=1, seqlen=150, nheads=4, headdim=64, dstate=64, rank=4, chunk=16, dt_shift=4.0),
 }
+
+
+@pytest.mark.parametrize("case", ["siso_strong_decay", "mimo4_strong_decay"])
+def test_strong_decay_cases_cover_both_decay_paths(case):
+    """The strong-decay cases really contain chunks on both sides of the
+    -60 log-decay threshold (chunk sums of dt * A in f32)."""
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], **SMALL[case])
+    inp = synth.prefill_inputs(wl)
+    dt = synth.to_f64(inp["dt"], wl.dtype).astype(np.float32)[0]  # [L][H]
+    A = inp["A"].astype(np.float32)
+    sums = []
+    for c0 in range(0, wl.seqlen, wl.chunk):
+        sums.append((dt[c0:c0 + wl.chunk] * A[None, :]).sum(0))
+    sums = np.concatenate(sums)
+    assert (sums <= -60).any() and (sums > -60).any(), sums
 
 
 @pytest.mark.parametrize("algo", ALGOS)
