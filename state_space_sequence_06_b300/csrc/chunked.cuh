@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
   using namespace umma;
 
   extern __shared__ uint8_t smem_raw[];
-  // barriers: full (TMA landed), opready (prologue done), free (stage no longer
+  // barriers: full (TMA landed), scal (per-token scalars of the chunk written:
+  // the state warps can weight X while the rotation runs), opready (prologue done), free (stage no longer
   // read by MMAs), xready (X of the slot's chunk converted), xfree (X slot and
   // output accumulators no longer read), sfull (MMA 1 done), yfull (MMAs 2
   // and 3 done), spready (S' written), scfull (MMA 4 done: the chunk-local
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
   // R).  A phase-parity wait is only sound when the waiter can never fall two
   // phases behind the barrier; each pairing below is chained so that it
   // cannot.
-  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
+  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2], bar_scal[2];
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB];
   __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_scfull, bar_scfree, bar_rfree;
   __shared__ uint32_t tmem_base_s;
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       mbar_init(saddr(&bar_free[s]), 2);   // MMA 1 and MMAs 4/3 completions
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
+      mbar_init(saddr(&bar_scal[s]), Q);   // the per-token weights of the chunk, one arrival per token
     }
     for (int x = 0; x < XB; ++x) {
       mbar_init(saddr(&bar_xfree[x]), 2);   // MMA 2 completion and the output epilogue
@@ -364,6 +366,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         sBw[xs][pt] = __expf(-lt) * wp;
         sELam[xs][pt] = __expf(lt);
         if (pt == 0) sLamEnd[xs] = lam_end;
+        mbar_arrive(saddr(&bar_scal[s]));  // theta is no longer read either
       }
       // ---- angle scan, part 2, and the in-place rotation of B and C by
       //      e^{-i Phi_i}, Phi_i = phase at the chunk start + chunk-local sum
@@ -548,12 +551,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       group_sync(2, NSTA);
       if (tt == 0) mbar_arrive(saddr(&bar_stready));
     }
-    // X of chunk c to f16 (slot c % XB) and W X as hi (over x) and lo parts:
-    // needs only the prologue of chunk c
+    // X of chunk c to f16 (slot c % XB) and W X as hi (over x) and lo (over
+    // theta, or its own area) parts: needs the landed X and the weights,
+    // which the prologue writes before it rotates B and C
     auto xconv = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
-      bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      if (got) got = wait_or_abort(saddr(&bar_scal[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(2, NSTA, got)) return false;
       {
@@ -838,15 +843,30 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
         if (s) ++issued1; else ++issued0;
       };
+      // the stage of chunk c + 2 frees only when chunk c is done; the chunk
+      // after it is fetched into L2 meanwhile, so its load then hits in L2
+      auto prefetch = [&](int c) {
+        if (c >= nchunks) return;
+        const int t = (int)(tok0 + (int64_t)c * Q);
+        tma_prefetch_4d(&tm_x, 0, 0, head, t);
+#pragma unroll
+        for (int kb = 0; kb < N / 64; ++kb) {
+          tma_prefetch_4d(&tm_B, 64 * kb, 0, head, t);
+          tma_prefetch_4d(&tm_C, 64 * kb, 0, head, t);
+        }
+        tma_prefetch_3d(&tm_th, 0, head, t);
+      };
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_B);
       tma_prefetch_desc(&tm_C);
       tma_prefetch_desc(&tm_th);
       issue(0);
       if (nchunks > 1) issue(1);
+      prefetch(2);
       for (int c = 0; c + 2 < nchunks; ++c) {
         if (!wait_or_abort(saddr(&bar_free[c & 1]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
         issue(c + 2);
+        prefetch(c + 3);
       }
       // every load issued must have landed before the CTA's shared memory goes away
       if (issued0 > 0) mbar_wait(saddr(&bar_full[0]), (uint32_t)((issued0 - 1) & 1), kMaxPolls);
