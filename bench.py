@@ -29,6 +29,7 @@ import synth  # noqa: E402
 
 METRIC = "Mamba-3 scan tokens/s (prefill) & decode steps/s; % of HBM/tensor roofline"
 L2_BYTES = 126 * 1024 ** 2
+PKG = "state_space_sequence_06_b300"
 
 
 def peaks():
@@ -64,12 +65,22 @@ def workload_bytes(wl) -> dict:
                 state=state, carry=carry, per_token_head=per_th_in + R * P * 4)
 
 
-def kernel_source_hash():
+# the sources each kernel is compiled from (its launcher included)
+KERNEL_SOURCES = {
+    "prefill": ["csrc/chunked.cuh", "csrc/recurrent.cuh", "csrc/umma.cuh", "csrc/common.cuh", "csrc/m3scan.cu",
+                "include/m3scan.h"],
+    "decode_step": ["csrc/decode.cuh", "csrc/umma.cuh", "csrc/common.cuh", "csrc/m3scan.cu", "include/m3scan.h"],
+}
+
+
+def kernel_source_hash(kind):
+    """Hash of the sources a kernel is built from: a committed DRAM-traffic
+    figure counts only while it matches."""
     h = hashlib.sha256()
-    for d in ("state_space_sequence_06_b300/csrc", "include"):
-        for fn in sorted(os.listdir(os.path.join(ROOT, d))):
-            with open(os.path.join(ROOT, d, fn), "rb") as f:
-                h.update(f.read())
+    for rel in KERNEL_SOURCES[kind]:
+        path = os.path.join(ROOT, rel if rel.startswith("include") else os.path.join(PKG, rel))
+        with open(path, "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -80,7 +91,7 @@ def traffic_for(kernel_key):
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         e = d.get(kernel_key)
-        if e and e.get("source_sha") == kernel_source_hash():
+        if e and e.get("source_sha") == kernel_source_hash(kernel_key.split(":")[0]):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
