@@ -46,9 +46,12 @@ def workload_bytes(wl) -> dict:
     the f32 state read (when it carries in) and written once."""
     isz = 2 if wl.dtype == "bf16" else 4
     H, P, N, R = wl.nheads, wl.headdim, wl.dstate, wl.rank
+    # per token and head: x, B, C, dt, and lam / theta unless they are the
+    # special values (not read at all then)
+    per_in = R * P + 2 * R * N + 1 + (0 if wl.euler else 1) + (0 if wl.real else N // 2)
     if wl.kind == "decode":
         units = wl.batch * H
-        per_step_in = units * (R * P + 2 * R * N + 2 + N // 2) * isz
+        per_step_in = units * per_in * isz
         carry = units * (R * N + R * P) * isz * 2  # read old, write new
         state = units * N * P * 4 * 2
         y = units * R * P * 4
@@ -56,7 +59,7 @@ def workload_bytes(wl) -> dict:
                     inputs=per_step_in, state=state, carry=carry, y=y)
     tokens = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
     th = tokens * H
-    per_th_in = (R * P + 2 * R * N + 2 + N // 2) * isz
+    per_th_in = per_in * isz
     nseq = wl.nseq if wl.kind == "varlen" else wl.batch
     state = nseq * H * N * P * 4 * 2  # h0 read + h_final write
     carry = nseq * H * (R * N + R * P) * isz * 2
@@ -263,6 +266,9 @@ def config_of(wl):
         c["chunk"] = wl.chunk
     if wl.kind == "varlen":
         c["nseq"] = wl.nseq
+    if wl.real or wl.euler:
+        c["special_case"] = "Mamba-2: " + ", ".join(
+            ([("theta = 0 (real state)")] if wl.real else []) + (["lam = 1 (first order)"] if wl.euler else []))
     return c
 
 
@@ -270,6 +276,8 @@ def config_of(wl):
 
 
 def dev_tensor(torch, a):
+    if a is None:  # lam = 1 / theta = 0
+        return None
     t = torch.from_numpy(np.ascontiguousarray(a))
     if a.dtype == np.uint16:
         t = t.view(torch.bfloat16)
@@ -304,9 +312,10 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
             px.copy_(px0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
+            lam, th = t["lam"], t["theta"]
             for i in range(T):
-                m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], t["lam"][i], t["theta"][i],
-                                  t["A"], t["D"], y, st)
+                m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], None if lam is None else lam[i],
+                                  None if th is None else th[i], t["A"], t["D"], y, st)
             e1.record(stream)
             ev_pairs.append((e0, e1))
 
@@ -445,8 +454,8 @@ def main():
     head = measure(wl, args, m3, torch, dist, world, local, stream, headline=True)
     others = []
     if not args.quick:
-        for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "decode_siso_b256", "decode_mimo4_b256",
-                     "tiny_f32"):
+        for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "mamba2_b8_l4096", "decode_siso_b256",
+                     "decode_mimo4_b256", "decode_mamba2_b256", "tiny_f32"):
             if name == args.workload:
                 continue
             sargs = argparse.Namespace(**vars(args))
@@ -522,7 +531,7 @@ def sampled_parity(wl, m3, t, y, st, cu, algo):
 def measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world):
     """The same metric through the public API from pinned host buffers: each
     step copies its inputs host -> device, runs the scan and copies y back."""
-    keys = ("x", "B", "C", "dt", "lam", "theta")
+    keys = tuple(k for k in ("x", "B", "C", "dt", "lam", "theta") if t[k] is not None)
     host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in keys}
     for k in keys:
         host[k].copy_(t[k])

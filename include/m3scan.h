@@ -30,6 +30,13 @@
  *     kernel traps.  A kernel that gives up a bounded wait records
  *     M3_ERR_TIMEOUT in a device status word that m3_device_status() reads.
  *   - x, B, C, theta, y and the state must be 16-byte aligned.
+ *   - Mamba-2 mode ("Together AI announces Mamba-3", section 1 table: the
+ *     first-order exponential-Euler rule of Mamba-2; section 2 table: a
+ *     real-valued state): `theta` may be NULL, meaning theta = 0 (every
+ *     pair is two independent real states, so N real states in all), and
+ *     `lam` may be NULL, meaning lam = 1 (h_t = a_t h_{t-1} + dt_t u_t: no
+ *     previous-token term).  With both NULL the scan is the first-order real
+ *     SSM of Mamba-2 with N states, on the same layouts.
  *   - Floating point: inputs are f32 or bf16 (in_dtype); dt, lam and theta
  *     share that type; A, D, y and the state are f32; all arithmetic is f32
  *     (tensor-core products take bf16 operands with f32 accumulation).
@@ -100,8 +107,8 @@ typedef struct m3_prefill_args {
   const void* B;     /* [batch][L][H][R][N]   in_dtype */
   const void* C;     /* [batch][L][H][R][N]   in_dtype */
   const void* dt;    /* [batch][L][H]         in_dtype, > 0 */
-  const void* lam;   /* [batch][L][H]         in_dtype, in [0, 1] */
-  const void* theta; /* [batch][L][H][N/2]    in_dtype */
+  const void* lam;   /* [batch][L][H]         in_dtype, in [0, 1]; NULL: lam = 1 */
+  const void* theta; /* [batch][L][H][N/2]    in_dtype; NULL: theta = 0        */
   const float* A;    /* [H] f32, < 0 */
   const float* D;    /* [H] f32 */
   const int32_t* cu_seqlens; /* device [nseq+1], nondecreasing, cu[0] = 0, cu[nseq] = L; or NULL */
@@ -116,8 +123,8 @@ typedef struct m3_decode_args {
   const void* B;     /* [batch][H][R][N] in_dtype */
   const void* C;     /* [batch][H][R][N] in_dtype */
   const void* dt;    /* [batch][H]       in_dtype */
-  const void* lam;   /* [batch][H]       in_dtype */
-  const void* theta; /* [batch][H][N/2]  in_dtype */
+  const void* lam;   /* [batch][H]       in_dtype; NULL: lam = 1   */
+  const void* theta; /* [batch][H][N/2]  in_dtype; NULL: theta = 0 */
   const float* A;    /* [H] f32 */
   const float* D;    /* [H] f32 */
   float* y;          /* [batch][H][R][P] f32 output */

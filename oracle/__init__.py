@@ -146,8 +146,9 @@ def prefill(inp: dict, *, batch, L, H, P, N, R, dtype, cu_seqlens=None, units=No
         np.asarray(h0, np.float64).reshape((nseq * H, K, P, 2))[sel]
     pB = per_unit(prev_B, (R, N))
     px = per_unit(prev_x, (R, P))
+    lam, theta = _lam_theta(inp, K)
     yflat, h, pB, px = run_units(tab, R, P, N, dtype, inp["x"], inp["B"], inp["C"], inp["dt"],
-                                 inp["lam"], inp["theta"], inp["A"], inp["D"], h, pB, px, yoff,
+                                 lam, theta, inp["A"], inp["D"], h, pB, px, yoff,
                                  nthreads=nthreads, lib=lib)
     if units is None:
         y = np.zeros((batch, L, H, R, P))
@@ -183,8 +184,9 @@ def decode(inp: dict, *, batch, H, P, N, R, dtype, steps, units=None, nthreads=N
     h = np.asarray(inp["h0"], np.float64).reshape(batch * H, K, P, 2)[sel]
     pB = _widen(inp["prev_B"], dtype).reshape(batch * H, R, N)[sel]
     px = _widen(inp["prev_x"], dtype).reshape(batch * H, R, P)[sel]
+    lam, theta = _lam_theta(inp, K)
     yflat, h, pB, px = run_units(tab, R, P, N, dtype, inp["x"], inp["B"], inp["C"], inp["dt"],
-                                 inp["lam"], inp["theta"], inp["A"], inp["D"], h, pB, px,
+                                 lam, theta, inp["A"], inp["D"], h, pB, px,
                                  len(sel) * steps * R * P, nthreads=nthreads, lib=lib)
     yu = yflat.reshape(len(sel), steps, R, P)
     if units is None:
@@ -192,6 +194,18 @@ def decode(inp: dict, *, batch, H, P, N, R, dtype, steps, units=None, nthreads=N
     else:
         y = {u: yu[i] for i, u in enumerate(sel)}
     return y, h.reshape(len(sel), K, P, 2), pB, px
+
+
+def _lam_theta(inp, K):
+    """lam and theta of ``inp``; None stands for lam = 1 and theta = 0 (the
+    first-order, real-state special case), written out as arrays."""
+    lam, theta = inp.get("lam"), inp.get("theta")
+    dt = np.asarray(inp["dt"])  # the C oracle reads every input in dt's storage type
+    if lam is None:
+        lam = np.full(dt.shape, 0x3F80, np.uint16) if dt.dtype == np.uint16 else np.ones(dt.shape, dt.dtype)
+    if theta is None:
+        theta = np.zeros(dt.shape + (K,), dt.dtype)
+    return lam, theta
 
 
 def _widen(a, dtype):

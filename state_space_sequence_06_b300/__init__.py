@@ -174,7 +174,8 @@ def m3_state_view(state: State) -> m3_state_ptrs:
 def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
                     cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None):
     """Prefill.  x [b][L][H][R][P], B/C [b][L][H][R][N], dt/lam [b][L][H],
-    theta [b][L][H][N/2] (all bf16 or all f32), A/D [H] f32, y [b][L][H][R][P]
+    theta [b][L][H][N/2] (all bf16 or all f32; lam None: lam = 1, theta
+    None: theta = 0), A/D [H] f32, y [b][L][H][R][P]
     f32 (written).  ``cu_seqlens`` (int32 CUDA tensor) packs sequences in a
     batch of one row."""
     b, L, H, R, P = x.shape
@@ -193,7 +194,8 @@ def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = N
 
 def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None):
     """One decode step.  x [b][H][R][P], B/C [b][H][R][N], dt/lam [b][H],
-    theta [b][H][N/2], A/D [H] f32, y [b][H][R][P] f32 (written)."""
+    theta [b][H][N/2] (lam / theta None: 1 / 0), A/D [H] f32, y [b][H][R][P]
+    f32 (written)."""
     b, H, R, P = x.shape
     N = B.shape[-1]
     a = m3_decode_args()

@@ -67,8 +67,12 @@ struct ChunkParams {
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-template <int N_, int R_, int Q_>
+// RE: theta = 0 (a real state, the Mamba-2 special case): B and C need no
+// rotation, convert to f16 exactly and carry no lo parts, and theta is not
+// loaded.
+template <int N_, int R_, int Q_, bool RE_ = false>
 struct ChunkCfg {
+  static constexpr bool RE = RE_;
   static constexpr int N = N_, R = R_, Q = Q_, P = 64;
   static constexpr int K2 = N / 2;  // complex pairs
   static constexpr int MR = Q * R;  // rows of S and Y: (token, rank)
@@ -100,7 +104,7 @@ struct ChunkCfg {
   static constexpr bool WXLO_IN_TH = TH_BYTES >= XT_BYTES;
   static constexpr int OFF_WXLO = WXLO_IN_TH ? OFF_TH : align_up(OFF_TH + TH_BYTES, 1024);
   static constexpr int STAGE = align_up(WXLO_IN_TH ? OFF_TH + TH_BYTES : OFF_WXLO + XT_BYTES, 1024);
-  static constexpr uint32_t STAGE_TX = 2 * CT_BYTES + XT_BYTES + TH_BYTES;
+  static constexpr uint32_t STAGE_TX = 2 * CT_BYTES + XT_BYTES + (RE ? 0 : TH_BYTES);
   // outside the stages: X in f16 (it lives until the output of its chunk,
   // so it and the per-chunk scalars rotate through XB slots: three when they
   // fit), S' hi and lo (K-major), R (MN-major)
@@ -192,12 +196,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return wait_or_abort_slow(bar, parity, abort_flag);
 }
 
-template <int N, int R, int Q>
-__global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
+template <int N, int R, int Q, bool RE>
+__global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                            const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_th,
                            const ChunkParams p) {
-  using Cfg = ChunkCfg<N, R, Q>;
+  using Cfg = ChunkCfg<N, R, Q, RE>;
   constexpr int P = Cfg::P, K2 = Cfg::K2, MR = Cfg::MR, NPRO = Cfg::NPRO, NSTA = Cfg::NSTA;
   constexpr int G = Cfg::G, TPG = Cfg::TPG, XB = Cfg::XB;
   using namespace umma;
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         const int64_t i = (int64_t)c * Q + pt;
         if (i < ntok) {
           d = __ldg(dt_bits + (tok0 + i) * H + head);
-          l = __ldg(lam_bits + (tok0 + i) * H + head);
+          l = lam_bits ? __ldg(lam_bits + (tok0 + i) * H + head) : 0x3F80u;  // no lam: lam = 1
         }
       }
     };
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       // ---- angle scan, part 1: per-group sums of dt * theta
       const __nv_bfloat16* th = reinterpret_cast<const __nv_bfloat16*>(stg + Cfg::OFF_TH);
       float om[TPG];
-      {
+      if (!RE) {
         float part = 0.f;
 #pragma unroll
         for (int ii = 0; ii < TPG; ++ii) {
@@ -371,7 +375,24 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
       // ---- angle scan, part 2, and the in-place rotation of B and C by
       //      e^{-i Phi_i}, Phi_i = phase at the chunk start + chunk-local sum
       float tot = 0.f;
-      {
+      if (RE) {  // theta = 0: B and C convert to f16 exactly, in place
+        uint8_t* Bt = stg + Cfg::OFF_B;
+        uint8_t* Ct = stg + Cfg::OFF_C;
+        const int blk = (2 * k) / 64, col = (2 * k) % 64;
+#pragma unroll
+        for (int ii = 0; ii < TPG; ++ii) {
+          const int i = g * TPG + ii;
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const uint32_t rc = sw128_offset(i * R + r, col);
+            const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
+            const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
+            const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
+            *reinterpret_cast<uint32_t*>(Bt + ob) = pack_half2(b.x, b.y);
+            *reinterpret_cast<uint32_t*>(Ct + o) = pack_half2(cc.x, cc.y);
+          }
+        }
+      } else {
         float off = 0.f;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
@@ -417,7 +438,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
         }
       }
       group_sync(1, NPRO);  // sDw ready; theta and sPhi fully read
-      if (g == 0) {         // advance the running phase by the chunk's angle, reduced to [-pi, pi)
+      if (!RE && g == 0) {  // advance the running phase by the chunk's angle, reduced to [-pi, pi)
         const float ph = sPhi[k] + tot;
         sPhi[k] = fmaf(-rintf(ph * 0.15915494309189535f), 6.283185307179586f, ph);
       }
@@ -518,7 +539,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
     // initial state: h'_{-1} = h0 + beta'_0 * sum_r Bprev_r xprev_r^T  (realified rows)
     {
       const float dt0 = __bfloat162float(p.dt[tok0 * H + head]);
-      const float lm0 = __bfloat162float(p.lam[tok0 * H + head]);
+      const float lm0 = p.lam ? __bfloat162float(p.lam[tok0 * H + head]) : 1.f;
       const float bet0 = (1.f - lm0) * dt0;
       for (int cb = 0; cb < P; cb += 16) {
         float v[16];
@@ -753,8 +774,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
 #pragma unroll 1
         for (int ks = 0; ks < N / 16; ++ks) {
           mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Bt, ks, Cfg::BB), idesc, ks > 0);
-          mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, Cfg::BB), idesc, 1);
-          mma_f16(d, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, Cfg::BB), idesc, 1);
+          if (!RE) {  // the lo parts of the rotated operands
+            mma_f16(d, kmaj(Ct, ks, MR * 128), kmaj(Blo, ks, Cfg::BB), idesc, 1);
+            mma_f16(d, kmaj(Clo, ks, MR * 128), kmaj(Bt, ks, Cfg::BB), idesc, 1);
+          }
         }
         mma_commit(saddr(&bar_sfull[s]));
         mma_commit(saddr(&bar_free[s]));
@@ -801,7 +824,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
 #pragma unroll 1
           for (int ks = 0; ks < N / 16; ++ks) {
             mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Ct, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, ks > 0);
-            mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
+            if (!RE)
+              mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
           }
         }
         mma_commit(saddr(&bar_rfree));
@@ -816,7 +840,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
           for (int ks = 0; ks < MR / 16; ++ks) {
             mma_f16(tmem + Cfg::COL_SC, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, ks > 0);
             mma_f16(tmem + Cfg::COL_SC, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXlo, ks, MR * 128), idesc, 1);
-            mma_f16(tmem + Cfg::COL_SC, mnmaj(Blo, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, 1);
+            if (!RE) mma_f16(tmem + Cfg::COL_SC, mnmaj(Blo, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, 1);
           }
         }
         // each commit tracks every product issued so far by this thread
@@ -840,7 +864,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
           tma_load_4d(saddr(stg + Cfg::OFF_B + kb * Cfg::BB), &tm_B, bar, 64 * kb, 0, head, t);
           tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head, t);
         }
-        tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
+        if (!RE) tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
         if (s) ++issued1; else ++issued0;
       };
       // the stage of chunk c + 2 frees only when chunk c is done; the chunk
@@ -854,12 +878,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q>::NT, 1)
           tma_prefetch_4d(&tm_B, 64 * kb, 0, head, t);
           tma_prefetch_4d(&tm_C, 64 * kb, 0, head, t);
         }
-        tma_prefetch_3d(&tm_th, 0, head, t);
+        if (!RE) tma_prefetch_3d(&tm_th, 0, head, t);
       };
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_B);
       tma_prefetch_desc(&tm_C);
-      tma_prefetch_desc(&tm_th);
+      if (!RE) tma_prefetch_desc(&tm_th);
       issue(0);
       if (nchunks > 1) issue(1);
       prefetch(2);
@@ -929,15 +953,20 @@ inline bool make_map_4d_sw128(CUtensorMap* m, const void* base, uint64_t inner, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int N, int R, int Q>
+template <int N, int R, int Q, bool RE>
 m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq, cudaStream_t s) {
-  using Cfg = ChunkCfg<N, R, Q>;
+  using Cfg = ChunkCfg<N, R, Q, RE>;
   const int H = a->dims.nheads;
   const uint64_t T = (uint64_t)a->seqlen * (a->cu_seqlens ? 1 : a->dims.batch);
   CUtensorMap mx, mB, mC, mth;
   if (!make_map_4d_sw128(&mx, a->x, 64, R, H, T, Q) || !make_map_4d_sw128(&mB, a->B, N, R, H, T, Q) ||
-      !make_map_4d_sw128(&mC, a->C, N, R, H, T, Q) || !make_map_3d(&mth, a->theta, N / 2, H, T, Q))
+      !make_map_4d_sw128(&mC, a->C, N, R, H, T, Q))
     return M3_ERR_CUDA;
+  if (RE) {
+    mth = mx;  // not read: theta = 0
+  } else if (!make_map_3d(&mth, a->theta, N / 2, H, T, Q)) {
+    return M3_ERR_CUDA;
+  }
   ChunkParams p{};
   p.x = static_cast<const __nv_bfloat16*>(a->x);
   p.B = static_cast<const __nv_bfloat16*>(a->B);
@@ -952,7 +981,7 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   p.prev_x = static_cast<__nv_bfloat16*>(prev_x);
   p.L = a->seqlen;
   p.H = H;
-  auto kern = chunked_prefill_kernel<N, R, Q>;
+  auto kern = chunked_prefill_kernel<N, R, Q, RE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;
   const int units = nseq * H;
@@ -961,21 +990,29 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
 }
 
 // Shapes with a chunked kernel: bf16 inputs, P = 64, and (N, R, chunk) in
-// {(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)}.
+// {(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)}; with
+// theta = 0 (NULL) in {(128, 1, 64), (64, 1, 64), (64, 4, 16)}.
 inline m3_status chunked_prefill(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq,
                                  cudaStream_t s) {
   const m3_dims& d = a->dims;
   if (d.in_dtype != M3_BF16 || d.headdim != 64) return M3_ERR_UNSUPPORTED;
   const int R = d.rank, N = d.dstate;
   const int Q = a->chunk > 0 ? a->chunk : (R == 1 ? 64 : 64 / R);
+  const bool re = a->theta == nullptr;
 #define M3_CH(NN, RR, QQ) \
-  if (N == NN && R == RR && Q == QQ) return chunked_launch<NN, RR, QQ>(a, h, prev_B, prev_x, nseq, s);
+  if (!re && N == NN && R == RR && Q == QQ) return chunked_launch<NN, RR, QQ, false>(a, h, prev_B, prev_x, nseq, s);
+#define M3_CH_RE(NN, RR, QQ) \
+  if (re && N == NN && R == RR && Q == QQ) return chunked_launch<NN, RR, QQ, true>(a, h, prev_B, prev_x, nseq, s);
+  M3_CH_RE(128, 1, 64)
+  M3_CH_RE(64, 1, 64)
+  M3_CH_RE(64, 4, 16)
   M3_CH(128, 1, 64)
   M3_CH(64, 1, 64)
   M3_CH(64, 4, 16)
   M3_CH(64, 2, 32)
   M3_CH(128, 2, 32)
 #undef M3_CH
+#undef M3_CH_RE
   return M3_ERR_UNSUPPORTED;
 }
 

@@ -87,9 +87,9 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
   const T* Cg = static_cast<const T*>(p.C) + (int64_t)unit * R * N;
   T* pBg = static_cast<T*>(p.prev_B) + (int64_t)unit * R * N;
   T* pxg = static_cast<T*>(p.prev_x) + (int64_t)unit * R * P;
-  const T* thg = static_cast<const T*>(p.theta) + (int64_t)unit * K;
+  const T* thg = p.theta ? static_cast<const T*>(p.theta) + (int64_t)unit * K : nullptr;
   const uint32_t rn_bytes = (uint32_t)(R * N * sizeof(T)), rp_bytes = (uint32_t)(R * P * sizeof(T));
-  const uint32_t th_bytes = (uint32_t)(K * sizeof(T));
+  const uint32_t th_bytes = p.theta ? (uint32_t)(K * sizeof(T)) : 0u;  // no theta: theta = 0
 
   // 1. start the copies first: the state is the traffic that matters, the
   //    per-unit inputs ride on the same barrier when their rows allow it.
@@ -105,11 +105,11 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
       bulk_g2s(saddr(rawPB), pBg, rn_bytes, saddr(&bar));
       bulk_g2s(saddr(rawX), xg, rp_bytes, saddr(&bar));
       bulk_g2s(saddr(rawPX), pxg, rp_bytes, saddr(&bar));
-      bulk_g2s(saddr(rawTh), thg, th_bytes, saddr(&bar));
+      if (th_bytes) bulk_g2s(saddr(rawTh), thg, th_bytes, saddr(&bar));
     }
   }
   const float dt = ldf(static_cast<const T*>(p.dt), unit);
-  const float lam = ldf(static_cast<const T*>(p.lam), unit);
+  const float lam = p.lam ? ldf(static_cast<const T*>(p.lam), unit) : 1.f;  // no lam: lam = 1
   const float A = p.A[head], D = p.D[head];
   const float decay = expf(dt * A);
   __syncthreads();  // the mbarrier initialisation is visible
@@ -140,7 +140,12 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
   }
   for (int k = tid; k < K; k += blockDim.x) {
     float sn, cs;
-    sincosf(dt * to_f(sTh[k]), &sn, &cs);
+    if (p.theta) {
+      sincosf(dt * to_f(sTh[k]), &sn, &cs);
+    } else {
+      sn = 0.f;
+      cs = 1.f;
+    }
     kd2[(size_t)k * 2 * KW] = make_float2(decay * cs, decay * sn);
   }
   __syncthreads();  // records staged; the old carry is no longer needed

@@ -226,8 +226,8 @@ m3_status m3_state_view(const m3_state* st, m3_state_ptrs* out) {
 
 m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
   if (!a || !st || !dims_ok(&a->dims) || !same_dims(a->dims, st->dims)) return M3_ERR_INVALID_ARG;
-  if (!a->x || !a->B || !a->C || !a->dt || !a->lam || !a->theta || !a->A || !a->D || !a->y)
-    return M3_ERR_INVALID_ARG;
+  // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
+  if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
       !aligned16(a->y))
     return M3_ERR_INVALID_ARG;
@@ -244,8 +244,8 @@ m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
 
 m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) {
   if (!a || !dims_ok(&a->dims) || a->seqlen < 0) return M3_ERR_INVALID_ARG;
-  if (!a->x || !a->B || !a->C || !a->dt || !a->lam || !a->theta || !a->A || !a->D || !a->y)
-    return M3_ERR_INVALID_ARG;
+  // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
+  if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
       !aligned16(a->y))
     return M3_ERR_INVALID_ARG;

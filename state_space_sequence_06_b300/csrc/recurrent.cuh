@@ -110,12 +110,12 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
       const int tb = i / K, k = i % K;
       const int64_t ts = (tok0 + t0 + tb) * H + head;
       const float dt = ldf(dtg, ts);
-      float s, c;
-      sincosf(dt * ldf(thg, ts * K + k), &s, &c);
+      float s = 0.f, c = 1.f;  // theta = 0 when theta is not given
+      if (thg) sincosf(dt * ldf(thg, ts * K + k), &s, &c);
       const float dec = expf(dt * A);
       al[tb * K + k] = make_float2(dec * c, dec * s);
       if (k == 0) {
-        const float lm = ldf(lmg, ts);
+        const float lm = lmg ? ldf(lmg, ts) : 1.f;  // lam = 1 when lam is not given
         sc[2 * tb] = lm * dt;
         sc[2 * tb + 1] = (1.f - lm) * dt;
       }

@@ -117,6 +117,8 @@ class Workload:
     len_lo: int = 0
     len_hi: int = 0
     seed: int = 0
+    real: bool = False   # theta = 0: a real state (given as None)
+    euler: bool = False  # lam = 1: first-order exponential Euler (given as None)
     cu_seqlens: np.ndarray | None = field(default=None, repr=False)
     # shard of a global problem: this shard's `batch` sequences (varlen:
     # `nseq` sequences) are number shard_index*batch.. of a global batch of
@@ -143,6 +145,12 @@ def workloads() -> dict:
             "decode_mimo4_b256", "decode", 256, 1024, 32, 64, 64, 4, "bf16", h0_std=0.1, carry=True
         ),
         "long_l16384": Workload("long_l16384", "prefill", 1, 16384, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0),
+        # the Mamba-2 special case on the same shapes: real state (theta = 0), first order (lam = 1)
+        "mamba2_b8_l4096": Workload("mamba2_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16", chunk=64,
+                                    real=True, euler=True),
+        "decode_mamba2_b256": Workload(
+            "decode_mamba2_b256", "decode", 256, 1024, 32, 64, 128, 1, "bf16", h0_std=0.1, carry=True,
+            real=True, euler=True),
         "varlen_16": Workload(
             "varlen_16", "varlen", 1, 0, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0,
             nseq=16, len_lo=256, len_hi=8192,
@@ -218,6 +226,10 @@ def prefill_inputs(wl: Workload) -> dict:
         "A": fill((H,), S_A, K_NEG_EXP, 0.0, 0.5, "f32", s),
         "D": fill((H,), S_D, K_NORMAL, 0.0, 1.0, "f32", s),
     }
+    if wl.real:
+        d["theta"] = None
+    if wl.euler:
+        d["lam"] = None
     nseq = wl.nseq if wl.kind == "varlen" else b
     if wl.h0_std > 0:
         d["h0"] = unit((nseq, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32")
@@ -269,6 +281,10 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
         "A": fill((H,), S_A, K_NEG_EXP, 0.0, 0.5, "f32", s),
         "D": fill((H,), S_D, K_NORMAL, 0.0, 1.0, "f32", s),
     }
+    if wl.real:
+        d["theta"] = None
+    if wl.euler:
+        d["lam"] = None
     if wl.h0_std > 0:
         d["h0"] = unit((b, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32")
     else:

@@ -11,8 +11,11 @@ import state_space_sequence_06_b300 as m3
 TOL = {"f32": 1e-4, "bf16": 1e-2}
 
 
-def dev(a: np.ndarray, dtype: str | None = None) -> torch.Tensor:
-    """numpy -> CUDA tensor; uint16 arrays are bf16 bit patterns."""
+def dev(a: np.ndarray | None, dtype: str | None = None) -> torch.Tensor | None:
+    """numpy -> CUDA tensor; uint16 arrays are bf16 bit patterns; None stays
+    None (an input the library treats as its special value)."""
+    if a is None:
+        return None
     t = torch.from_numpy(np.ascontiguousarray(a))
     if a.dtype == np.uint16:
         t = t.view(torch.bfloat16)

@@ -31,11 +31,14 @@ def run_decode(wl, steps, units=None, window=None):
         t = {k: dev(d[k]) for k in ("x", "B", "C", "dt", "lam", "theta")}
         A, D = dev(d["A"]), dev(d["D"])
         for i in range(n):
-            m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], t["lam"][i], t["theta"][i],
-                              A, D, y, st)
+            lam_i = None if t["lam"] is None else t["lam"][i]
+            th_i = None if t["theta"] is None else t["theta"][i]
+            m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], lam_i, th_i, A, D, y, st)
             sumsq += (y.double() ** 2).sum()
             ys.append(y.reshape(b * H, R, P)[sel].cpu().numpy())
         for k in ("x", "B", "C", "dt", "lam", "theta"):
+            if d[k] is None:  # lam = 1 / theta = 0: the oracle takes None the same way
+                continue
             v = d[k].reshape((n, b * H) + d[k].shape[3:])[:, sel] if k not in ("dt", "lam") else \
                 d[k].reshape(n, b * H)[:, sel]
             allin.setdefault(k, []).append(v)
@@ -53,10 +56,11 @@ def run_decode(wl, steps, units=None, window=None):
     T = steps
     sub = dict(x=sub["x"].reshape(T, len(sel), 1, R, P), B=sub["B"].reshape(T, len(sel), 1, R, N),
                C=sub["C"].reshape(T, len(sel), 1, R, N), dt=sub["dt"].reshape(T, len(sel), 1),
-               lam=sub["lam"].reshape(T, len(sel), 1), theta=sub["theta"].reshape(T, len(sel), 1, N // 2))
+               lam=sub["lam"].reshape(T, len(sel), 1) if "lam" in sub else None,
+               theta=sub["theta"].reshape(T, len(sel), 1, N // 2) if "theta" in sub else None)
     yo, ho, pBo, pxo = [], [], [], []
     for i, u in enumerate(sel):
-        one = {k: np.ascontiguousarray(v[:, i:i + 1]) for k, v in sub.items()}
+        one = {k: (None if v is None else np.ascontiguousarray(v[:, i:i + 1])) for k, v in sub.items()}
         one["A"] = init["A"][heads[i]:heads[i] + 1]
         one["D"] = init["D"][heads[i]:heads[i] + 1]
         one["h0"] = init["h0"].reshape(b * H, N // 2, P, 2)[u:u + 1]
