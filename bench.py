@@ -454,8 +454,9 @@ def main():
     head = measure(wl, args, m3, torch, dist, world, local, stream, headline=True)
     others = []
     if not args.quick:
-        for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "mamba2_b8_l4096", "decode_siso_b256",
-                     "decode_mimo4_b256", "decode_mamba2_b256", "tiny_f32"):
+        for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "siso_n64_b8_l4096", "mamba2_b8_l4096",
+                     "decode_siso_b256", "decode_mimo4_b256", "decode_siso_n64_b256", "decode_mamba2_b256",
+                     "tiny_f32"):
             if name == args.workload:
                 continue
             sargs = argparse.Namespace(**vars(args))

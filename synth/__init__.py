@@ -145,6 +145,11 @@ def workloads() -> dict:
             "decode_mimo4_b256", "decode", 256, 1024, 32, 64, 64, 4, "bf16", h0_std=0.1, carry=True
         ),
         "long_l16384": Workload("long_l16384", "prefill", 1, 16384, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0),
+        # Mamba-3 with half the state (N 64: 32 complex pairs), the size at which the pages report
+        # Mamba-2's N 128 perplexity
+        "siso_n64_b8_l4096": Workload("siso_n64_b8_l4096", "prefill", 8, 4096, 32, 64, 64, 1, "bf16", chunk=64),
+        "decode_siso_n64_b256": Workload(
+            "decode_siso_n64_b256", "decode", 256, 1024, 32, 64, 64, 1, "bf16", h0_std=0.1, carry=True),
         # the Mamba-2 special case on the same shapes: real state (theta = 0), first order (lam = 1)
         "mamba2_b8_l4096": Workload("mamba2_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16", chunk=64,
                                     real=True, euler=True),
