@@ -63,7 +63,23 @@ struct ChunkParams {
   __nv_bfloat16* prev_x;
   int64_t L;
   int H;
+  // Balanced schedule (bal_grid == 0: one CTA per (sequence, head) unit).
+  // With fixed-length sequences the bal_units units' chunks, unit after
+  // unit, are cut into bal_grid equal ranges, one per CTA (all resident at
+  // once: a cooperative launch).  A unit cut by the boundary before CTA k is
+  // a prefill of its first chunks in CTA k - 1 (run first there) followed by
+  // a prefill of the rest in CTA k (run last there) from the state and carry
+  // handed over through slot k.
+  int bal_grid;
+  int bal_units;
+  float* xh;             // handover h [slot][K2][P][2]
+  __nv_bfloat16* xB;     // handover carry [slot][R][N]
+  __nv_bfloat16* xx;     // handover carry [slot][R][P]
+  int* xflag;            // [slot]: 1 once the slot is written (zeroed before the launch)
 };
+
+constexpr int kMaxSeg = 8;  // segments per CTA in a balanced schedule
+constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2;
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -207,8 +223,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   using namespace umma;
 
   extern __shared__ uint8_t smem_raw[];
-  // barriers: full (TMA landed), scal (per-token scalars of the chunk written:
-  // the state warps can weight X while the rotation runs), opready (prologue done), free (stage no longer
+  // barriers: full (TMA landed), phend (the phase after the chunk written,
+  // read where a segment ends), opready (prologue done), free (stage no longer
   // read by MMAs), xready (X of the slot's chunk converted), xfree (X slot and
   // output accumulators no longer read), sfull (MMA 1 done), yfull (MMAs 2
   // and 3 done), spready (S' written), scfull (MMA 4 done: the chunk-local
@@ -218,8 +234,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   // R).  A phase-parity wait is only sound when the waiter can never fall two
   // phases behind the barrier; each pairing below is chained so that it
   // cannot.
-  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2], bar_scal[2];
-  __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB];
+  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
+  __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB], bar_phend[XB];
   __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_scfull, bar_scfree, bar_rfree;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_abort[1];  // this CTA's abort flag
@@ -230,23 +246,81 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   __shared__ float sDt[Q + 1], sBet[Q + 1], sWarpTot[4];
   __shared__ float sPsum[G][K2];
   __shared__ float sPhi[K2];  // cumulative angle per pair at the end of the last chunk, in [-pi, pi)
+  __shared__ float sPhiEndX[XB][K2];  // the same after chunk c (slot c % XB), for the state warps
+
+  // this CTA's segments: {unit, first token, end token, flags}, the first
+  // chunk of each in the CTA's chunk stream, and the first token's row
+  __shared__ int4 sSeg[kMaxSeg];
+  __shared__ int sSegC0[kMaxSeg + 1];
+  __shared__ long long sSegTok0[kMaxSeg];
+  __shared__ int sSegHead[kMaxSeg];
+  __shared__ float sSegA[kMaxSeg], sSegD[kMaxSeg];  // the head's A and D (read once, not per chunk)
+  __shared__ int sNseg;
 
   uint8_t* sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int unit = blockIdx.x;
   const int H = p.H;
-  const int seq = unit / H, head = unit % H;
-  int64_t tok0, ntok;
-  if (p.cu_seqlens) {
-    tok0 = p.cu_seqlens[seq];
-    ntok = (int64_t)p.cu_seqlens[seq + 1] - tok0;
-  } else {
-    tok0 = (int64_t)seq * p.L;
-    ntok = p.L;
+  if (tid == 0) {
+    int ns = 0;
+    if (p.bal_grid) {
+      const int64_t nch = (p.L + Q - 1) / Q, total = (int64_t)p.bal_units * nch;
+      const int k = blockIdx.x;
+      const int64_t lo = k * total / p.bal_grid, hi = (k + 1) * total / p.bal_grid;
+      // head: the first part of a unit whose rest CTA k + 1 runs (first here);
+      // tail: the rest of a unit CTA k - 1 started (last here)
+      int4 head_seg = make_int4(0, 0, 0, -1), tail_seg = make_int4(0, 0, 0, -1);
+      int4 mid[kMaxSeg];
+      int nmid = 0;
+      for (int64_t u = lo / nch; u * nch < hi; ++u) {
+        const int64_t cb = lo > u * nch ? lo : u * nch, ce = hi < (u + 1) * nch ? hi : (u + 1) * nch;
+        const int tb = (int)((cb - u * nch) * Q);
+        const int te = (int)((ce - u * nch) * Q < p.L ? (ce - u * nch) * Q : p.L);
+        int4 sg = make_int4((int)u, tb, te, 0);
+        if (cb > u * nch) {
+          sg.w = SEG_SRC_SLOT | (k << 8);
+          tail_seg = sg;
+        } else if (ce < (u + 1) * nch) {
+          sg.w = SEG_DST_SLOT | ((k + 1) << 8);
+          head_seg = sg;
+        } else if (nmid < kMaxSeg - 2) {  // (the host keeps a CTA's whole units to kMaxSeg - 2)
+          mid[nmid++] = sg;
+        }
+      }
+      if (head_seg.w >= 0) sSeg[ns++] = head_seg;
+      for (int i = 0; i < nmid; ++i) sSeg[ns++] = mid[i];
+      if (tail_seg.w >= 0) sSeg[ns++] = tail_seg;
+    } else {
+      const int u = blockIdx.x, sq = u / H;
+      const int n = p.cu_seqlens ? p.cu_seqlens[sq + 1] - p.cu_seqlens[sq] : (int)p.L;
+      if (n > 0) sSeg[ns++] = make_int4(u, 0, n, 0);
+    }
+    int c0 = 0;
+    for (int i = 0; i < ns; ++i) {
+      const int sq = sSeg[i].x / H;
+      const long long base = p.cu_seqlens ? (long long)p.cu_seqlens[sq] : (long long)sq * p.L;
+      sSegTok0[i] = base + sSeg[i].y;
+      sSegHead[i] = sSeg[i].x % H;
+      sSegA[i] = p.A[sSeg[i].x % H];
+      sSegD[i] = p.D[sSeg[i].x % H];
+      sSegC0[i] = c0;
+      c0 += (sSeg[i].z - sSeg[i].y + Q - 1) / Q;
+    }
+    sSegC0[ns] = c0;
+    sNseg = ns;
   }
-  if (ntok <= 0) return;  // nothing to do; the state slot keeps its contents
-  const int nchunks = (int)((ntok + Q - 1) / Q);
-  const float A = p.A[head];
+  __syncthreads();
+  const int nseg = sNseg;
+  const int nchunks = sSegC0[nseg];
+  if (nchunks == 0) return;  // nothing to do; the state slot keeps its contents
+  // segment of chunk c of this CTA's stream (a handful of entries)
+  auto seg_of = [&](int c) {
+    int si = 0;
+    while (si + 1 < nseg && c >= sSegC0[si + 1]) ++si;
+    return si;
+  };
+  auto seg_head = [&](int si) { return sSegHead[si]; };
+  auto seg_ntok = [&](int si) { return (int64_t)(sSeg[si].z - sSeg[si].y); };
+  auto seg_last = [&](int c) { return c + 1 == sSegC0[seg_of(c) + 1]; };
   volatile int* abort_flag = s_abort;
 
   uint8_t* St = sm + Cfg::OFF_ST;
@@ -267,11 +341,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       mbar_init(saddr(&bar_free[s]), 2);   // MMA 1 and MMAs 4/3 completions
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
-      mbar_init(saddr(&bar_scal[s]), Q);   // the per-token weights of the chunk, one arrival per token
     }
     for (int x = 0; x < XB; ++x) {
       mbar_init(saddr(&bar_xfree[x]), 2);   // MMA 2 completion and the output epilogue
       mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X
+      mbar_init(saddr(&bar_phend[x]), K2);  // the phase after the slot's chunk, one arrival per pair
     }
     mbar_init(saddr(&bar_spready), 1);
     mbar_init(saddr(&bar_stready), 1);
@@ -294,20 +368,23 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     const int pt = tid;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const int k = pt % K2, g = pt / K2;  // rotation: pair k for the tokens of group g
-    if (pt < K2) sPhi[pt] = 0.f;
     // dt and lam of token pt of a chunk (token Q: the next chunk's first),
     // loaded one chunk ahead as raw bf16 bits: converting them only where
     // they are used keeps the load latency behind a whole chunk of work
     const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(p.dt);
     const unsigned short* lam_bits = reinterpret_cast<const unsigned short*>(p.lam);
+    // (token Q of the last chunk of a segment lies past its end: zero, the
+    // carry takes the next token's previous-token term)
     auto load_scalars = [&](int c, uint32_t& d, uint32_t& l) {
       d = 0u;
       l = 0u;
       if (pt <= Q && c < nchunks) {
-        const int64_t i = (int64_t)c * Q + pt;
-        if (i < ntok) {
-          d = __ldg(dt_bits + (tok0 + i) * H + head);
-          l = lam_bits ? __ldg(lam_bits + (tok0 + i) * H + head) : 0x3F80u;  // no lam: lam = 1
+        const int si = seg_of(c);
+        const int64_t i = (int64_t)(c - sSegC0[si]) * Q + pt;
+        if (i < seg_ntok(si)) {
+          const int64_t row = (sSegTok0[si] + i) * H + seg_head(si);
+          d = __ldg(dt_bits + row);
+          l = lam_bits ? __ldg(lam_bits + row) : 0x3F80u;  // no lam: lam = 1
         }
       }
     };
@@ -318,6 +395,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     auto prologue = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
+      const int si = seg_of(c);
+      const float A = sSegA[si];
+      // a segment starts from the phase 0 (its initial state is un-rotated);
+      // these threads also wrote the previous chunk's phase
+      if (c == sSegC0[si] && pt < K2) sPhi[pt] = 0.f;
       uint32_t d_nxt, l_nxt;
       load_scalars(c + 1, d_nxt, l_nxt);
       bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
@@ -370,11 +452,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         sBw[xs][pt] = __expf(-lt) * wp;
         sELam[xs][pt] = __expf(lt);
         if (pt == 0) sLamEnd[xs] = lam_end;
-        mbar_arrive(saddr(&bar_scal[s]));  // theta is no longer read either
+      }
+      if (RE && g == 0) {  // theta = 0: the phase stays 0
+        sPhiEndX[xs][k] = sPhi[k];
+        mbar_arrive_warp(saddr(&bar_phend[xs]));
       }
       // ---- angle scan, part 2, and the in-place rotation of B and C by
       //      e^{-i Phi_i}, Phi_i = phase at the chunk start + chunk-local sum
-      float tot = 0.f;
       if (RE) {  // theta = 0: B and C convert to f16 exactly, in place
         uint8_t* Bt = stg + Cfg::OFF_B;
         uint8_t* Ct = stg + Cfg::OFF_C;
@@ -394,12 +478,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         }
       } else {
         float off = 0.f;
+        float tot = 0.f;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
           const float sv = sPsum[gg][k];
           off += (gg < g) ? sv : 0.f;
           tot += sv;
         }
+        const float ph_end = sPhi[k] + tot;
         uint8_t* Bt = stg + Cfg::OFF_B;
         uint8_t* Ct = stg + Cfg::OFF_C;
         uint8_t* Blo = stg + Cfg::OFF_BLO;
@@ -436,12 +522,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             *reinterpret_cast<uint32_t*>(Clo + o) = lo;
           }
         }
+        if (g == 0) {  // the running phase after this chunk, reduced to [-pi, pi)
+          sPhiEndX[xs][k] = fmaf(-rintf(ph_end * 0.15915494309189535f), 6.283185307179586f, ph_end);
+          mbar_arrive_warp(saddr(&bar_phend[xs]));
+        }
       }
       group_sync(1, NPRO);  // sDw ready; theta and sPhi fully read
-      if (!RE && g == 0) {  // advance the running phase by the chunk's angle, reduced to [-pi, pi)
-        const float ph = sPhi[k] + tot;
-        sPhi[k] = fmaf(-rintf(ph * 0.15915494309189535f), 6.283185307179586f, ph);
-      }
+      if (g == 0) sPhi[k] = sPhiEndX[xs][k];  // advance the running phase (same thread wrote it)
       fence_async_smem();
       group_sync(1, NPRO);
       if (pt == 0) mbar_arrive(saddr(&bar_opready[s]));
@@ -535,31 +622,62 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     const int q4 = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int g_row = acc_row_of(N, q4, lane);  // state row owned by this thread (-1: none)
-    const float Dh = p.D[head];
-    // initial state: h'_{-1} = h0 + beta'_0 * sum_r Bprev_r xprev_r^T  (realified rows)
-    {
-      const float dt0 = __bfloat162float(p.dt[tok0 * H + head]);
-      const float lm0 = p.lam ? __bfloat162float(p.lam[tok0 * H + head]) : 1.f;
+    // initial state of segment si: h'_{-1} = h0 + beta'_0 * sum_r Bprev_r
+    // xprev_r^T (realified rows), h0 and the carry from the caller's state
+    // (zero without one) or from a handover slot, whose writer publishes it
+    // with a release store of its flag; also R = f16(G') for the first MMA 3
+    // of the segment.
+    auto init_seg = [&](int si) -> bool {
+      const int4 sg = sSeg[si];
+      const int unit = sg.x, head = unit % H;
+      const bool from_slot = (sg.w & SEG_SRC_SLOT) != 0;
+      const int slot = sg.w >> 8;
+      if (from_slot) {  // bounded wait for the CTA that runs the first part of this unit
+        bool ok = false;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 0; i < kMaxPolls; ++i) {
+          int f;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(p.xflag + slot) : "memory");
+          if (f) {
+            ok = true;
+            break;
+          }
+          if ((i & 63u) == 0 && (abort_flag[0] || globaltimer_ns() - t0 > kWaitLimitNs)) break;
+        }
+        if (!group_and(2, NSTA, ok)) {
+          if (tt == 0) {
+            abort_flag[0] = 1;
+            atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
+          }
+          return false;
+        }
+      }
+      const float* h0 = from_slot ? p.xh + (int64_t)slot * K2 * P * 2 : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr);
+      const __nv_bfloat16* cB = from_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
+      const __nv_bfloat16* cx = from_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
+      const int64_t row0 = sSegTok0[si] * H + head;
+      const float dt0 = __bfloat162float(p.dt[row0]);
+      const float lm0 = p.lam ? __bfloat162float(p.lam[row0]) : 1.f;
       const float bet0 = (1.f - lm0) * dt0;
       for (int cb = 0; cb < P; cb += 16) {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        if (g_row >= 0 && p.h) {
-          const float* hs = p.h + ((int64_t)unit * K2 + (g_row >> 1)) * P * 2 + (g_row & 1);
+        if (g_row >= 0 && h0) {
+          const float* hs = h0 + (int64_t)(g_row >> 1) * P * 2 + (g_row & 1);
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2];
-          if (p.prev_B) {
+          if (cB) {
             for (int r = 0; r < R; ++r) {
-              const float b = bet0 * __bfloat162float(p.prev_B[((int64_t)unit * R + r) * N + g_row]);
-              const __nv_bfloat16* xp = p.prev_x + ((int64_t)unit * R + r) * P + cb;
+              const float b = bet0 * __bfloat162float(cB[r * N + g_row]);
+              const __nv_bfloat16* xp = cx + r * P + cb;
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = fmaf(b, __bfloat162float(xp[i]), v[i]);
             }
           }
         }
         tmem_st16(tmem + lane_base + Cfg::COL_G + cb, v);
-        if (g_row >= 0) {  // R = f16(G') for MMA 3 of chunk 0
+        if (g_row >= 0) {  // R = f16(G') for MMA 3 of the segment's first chunk
 #pragma unroll
           for (int pc = 0; pc < 16; pc += 8)
             *reinterpret_cast<uint4*>(Rt + sw128_offset(g_row, cb + pc)) =
@@ -569,24 +687,71 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       }
       tmem_st_wait();
       fence_async_smem();
+      tc_fence_before();
       group_sync(2, NSTA);
       if (tt == 0) mbar_arrive(saddr(&bar_stready));
-    }
+      return true;
+    };
+    // final state of segment si (h of its last token, rotated back by the
+    // phase after its last chunk c) and carry (that token's B and x), to the
+    // caller's state or to a handover slot (then published with a release
+    // store of the slot's flag)
+    auto finalize = [&](int si, int c) {
+      const int4 sg = sSeg[si];
+      const int unit = sg.x, head = unit % H;
+      const bool to_slot = (sg.w & SEG_DST_SLOT) != 0;
+      const int slot = sg.w >> 8;
+      float* hd = to_slot ? p.xh + (int64_t)slot * K2 * P * 2 : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr);
+      __nv_bfloat16* cB = to_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
+      __nv_bfloat16* cx = to_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
+      if (hd) {  // h = e^{i Phi_end} G' (pairs of rows are (re, im) in adjacent lanes)
+        // the prologue of chunk c + XB (the slot's next writer) needs the
+        // output of chunk c, which follows: this parity wait cannot fall behind
+        if (!wait_or_abort(saddr(&bar_phend[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) return;
+        float cs = 1.f, sn = 0.f;
+        if (g_row >= 0) sincosf(sPhiEndX[c % XB][g_row >> 1], &sn, &cs);
+        const bool re = (g_row & 1) == 0;
+        for (int cb = 0; cb < P; cb += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
+            v[i] = re ? (cs * v[i] - sn * other) : (sn * other + cs * v[i]);
+          }
+          if (g_row >= 0) {
+            float* hs = hd + (int64_t)(g_row >> 1) * P * 2 + (g_row & 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) hs[(cb + i) * 2] = v[i];
+          }
+        }
+      }
+      if (cB) {
+        const int64_t last = (sSegTok0[si] + seg_ntok(si) - 1) * H + head;
+        for (int i = tt; i < R * N; i += NSTA) cB[i] = p.B[last * R * N + i];
+        for (int i = tt; i < R * P; i += NSTA) cx[i] = p.x[last * R * P + i];
+      }
+      if (to_slot) {
+        __threadfence();
+        group_sync(2, NSTA);
+        if (tt == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.xflag + slot), "r"(1) : "memory");
+      }
+    };
     // X of chunk c to f16 (slot c % XB) and W X as hi (over x) and lo (over
-    // theta, or its own area) parts: needs the landed X and the weights,
-    // which the prologue writes before it rotates B and C
+    // theta, or its own area) parts: after the prologue of chunk c (its
+    // weights, and its last read of theta)
     auto xconv = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
-      bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
-      if (got) got = wait_or_abort(saddr(&bar_scal[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(2, NSTA, got)) return false;
       {
         uint8_t* Xs = stg + Cfg::OFF_X;
         uint8_t* WXlo = stg + Cfg::OFF_WXLO;
         uint8_t* Xb = xbuf(xs);
-#pragma unroll 4
+#pragma unroll 2
         for (int idx = tt; idx < MR * (P / 8); idx += NSTA) {
           const int row = idx / (P / 8), c8 = idx % (P / 8);
           const uint32_t o = sw128_offset(row, c8 * 8);
@@ -612,9 +777,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     };
     // state step of chunk c, in the rotating frame: G' <- e^{Lam_end} G' + S_c
     // (S_c from MMA 4 of chunk c), then R = f16(G') for MMA 3 of chunk c + 1
-    // once MMA 3 of chunk c has read the previous R
+    // once MMA 3 of chunk c has read the previous R.  After the last chunk of
+    // a segment the next segment's initial state provides that R instead.
     auto state = [&](int c) -> bool {
       const int xs = c % XB;
+      const bool pub = !seg_last(c);
       bool got = wait_or_abort(saddr(&bar_scfull), (uint32_t)(c & 1), abort_flag);
       if (got) got = wait_or_abort(saddr(&bar_rfree), (uint32_t)(c & 1), abort_flag);
       if (!group_and(2, NSTA, got)) return false;
@@ -629,7 +796,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) g[i] = fmaf(elam_end, g[i], sc[i]);
         tmem_st16(tmem + lane_base + Cfg::COL_G + hc, g);
-        if (g_row >= 0) {
+        if (pub && g_row >= 0) {
 #pragma unroll
           for (int pc = 0; pc < 16; pc += 8)
             *reinterpret_cast<uint4*>(Rt + sw128_offset(g_row, hc + pc)) =
@@ -642,16 +809,21 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       tc_fence_before();
       group_sync(2, NSTA);
       if (tt == 0) {
-        mbar_arrive(saddr(&bar_stready));
+        if (pub) mbar_arrive(saddr(&bar_stready));
         mbar_arrive(saddr(&bar_scfree));
       }
       return true;
     };
+
     // output of chunk c: y = Y + e^{Lam_t} Yi + D x, needs MMAs 2 and 3 of chunk c
     auto output = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
-      const int64_t ct0 = tok0 + (int64_t)c * Q;
-      const int nvalid = (ntok - (int64_t)c * Q < Q) ? (int)(ntok - (int64_t)c * Q) : Q;
+      const int si = seg_of(c), head = seg_head(si);
+      const int64_t cc = c - sSegC0[si];
+      const int64_t ct0 = sSegTok0[si] + cc * Q;
+      const int64_t left = seg_ntok(si) - cc * Q;
+      const int nvalid = left < Q ? (int)left : Q;
+      const float Dh = sSegD[si];
       if (!group_and(2, NSTA, wait_or_abort(saddr(&bar_yfull[s]), (uint32_t)((c >> 1) & 1), abort_flag)))
         return false;
       tc_fence_after();
@@ -704,50 +876,28 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (tt == 0) mbar_arrive(saddr(&bar_xfree[xs]));
       return true;
     };
-    // order: X of chunk c + 1 as soon as its prologue is done, the output of
-    // chunk c (after its MMAs 2 and 3), then the state step of chunk c + 1,
-    // whose R the next MMA 3 needs long before its stage is released
-    bool alive = xconv(0) && state(0);
-    for (int c = 0; c < nchunks && alive; ++c) {
-      if (c + 1 < nchunks && !xconv(c + 1)) {
-        alive = false;
-        break;
-      }
-      if (!output(c)) {
-        alive = false;
-        break;
-      }
-      if (c + 1 < nchunks) alive = state(c + 1);
-    }
-    // ---- final state (h of the last token) and carry (the last token's B and x);
-    // `alive` is the same in every state warp (each step ends in a group vote)
-    if (alive) {
-      if (p.h) {  // h = e^{i Phi_end} G' (pairs of rows are (re, im) in adjacent lanes)
-        float cs = 1.f, sn = 0.f;
-        if (g_row >= 0) sincosf(sPhi[g_row >> 1], &sn, &cs);
-        const bool re = (g_row & 1) == 0;
-        for (int cb = 0; cb < P; cb += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
-            v[i] = re ? (cs * v[i] - sn * other) : (sn * other + cs * v[i]);
-          }
-          if (g_row >= 0) {
-            float* hs = p.h + ((int64_t)unit * K2 + (g_row >> 1)) * P * 2 + (g_row & 1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) hs[(cb + i) * 2] = v[i];
-          }
+    // order, chunk n after chunk: X of chunk n as soon as its prologue is
+    // done, the output of chunk n - 1 (after its MMAs 2 and 3), then the
+    // state step of chunk n (its R is needed by the next MMA 3 long before
+    // the stage is released).  A segment's initial state is loaded before
+    // its first chunk and its final state written after its last, outside
+    // the per-chunk loop, whose code stays small and contiguous (the roles
+    // of one SM share its instruction cache).  `alive` is the same in every
+    // state warp: each step ends in a group vote.
+    bool alive = true;
+    int n = 0;
+    for (int si = 0; si < nseg && alive; ++si) {
+      if (!init_seg(si)) break;
+      const int end = sSegC0[si + 1];
+      for (; n < end; ++n) {
+        if (!xconv(n) || (n >= 1 && !output(n - 1)) || !state(n)) {
+          alive = false;
+          break;
         }
       }
-      if (p.prev_B) {
-        const int64_t last = (tok0 + ntok - 1) * H + head;
-        for (int i = tt; i < R * N; i += NSTA) p.prev_B[(int64_t)unit * R * N + i] = p.B[last * R * N + i];
-        for (int i = tt; i < R * P; i += NSTA) p.prev_x[(int64_t)unit * R * P + i] = p.x[last * R * P + i];
-      }
+      if (alive) finalize(si, n - 1);
     }
+    if (alive) output(nchunks - 1);
   } else if (warp == Cfg::W_MMA || warp == Cfg::W_MMA2) {
     // ======================= MMA warps (one thread each issues)
     // K-major operand tiles: 16-element K step = 32 B inside a 128 B row, 64-column blocks MR*128 B apart
@@ -856,7 +1006,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         const int s = c & 1;
         uint8_t* stg = stage(s);
         const uint32_t bar = saddr(&bar_full[s]);
-        const int t = (int)(tok0 + (int64_t)c * Q);
+        const int si = seg_of(c), head = seg_head(si);
+        const int t = (int)(sSegTok0[si] + (int64_t)(c - sSegC0[si]) * Q);
         mbar_arrive_expect_tx(bar, Cfg::STAGE_TX);
         tma_load_4d(saddr(stg + Cfg::OFF_X), &tm_x, bar, 0, 0, head, t);
 #pragma unroll
@@ -871,7 +1022,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       // after it is fetched into L2 meanwhile, so its load then hits in L2
       auto prefetch = [&](int c) {
         if (c >= nchunks) return;
-        const int t = (int)(tok0 + (int64_t)c * Q);
+        const int si = seg_of(c), head = seg_head(si);
+        const int t = (int)(sSegTok0[si] + (int64_t)(c - sSegC0[si]) * Q);
         tma_prefetch_4d(&tm_x, 0, 0, head, t);
 #pragma unroll
         for (int kb = 0; kb < N / 64; ++kb) {
@@ -953,6 +1105,31 @@ inline bool make_map_4d_sw128(CUtensorMap* m, const void* base, uint64_t inner, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Stream-ordered memory for the balanced schedule's handover slots: a pool
+// per device owned by the library that keeps what it has allocated (a few
+// MB), so a call does not map fresh memory after every synchronisation.
+inline cudaMemPool_t handover_pool(int dev) {
+  static cudaMemPool_t pools[64] = {};
+  static bool tried[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!tried[dev]) {
+    tried[dev] = true;
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+      uint64_t keep = ~0ull;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      pools[dev] = pool;
+    } else {
+      cudaGetLastError();
+    }
+  }
+  return pools[dev];
+}
+
 template <int N, int R, int Q, bool RE>
 m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq, cudaStream_t s) {
   using Cfg = ChunkCfg<N, R, Q, RE>;
@@ -985,6 +1162,48 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;
   const int units = nseq * H;
+  // Balanced schedule: with more units than SMs, one CTA per unit leaves the
+  // last wave partly empty (256 units on 148 SMs: the second wave is 73 %
+  // full).  Instead every SM gets an equal range of the chunks, cutting at
+  // most one unit at each end; fixed-length sequences only, a few whole
+  // units per CTA at most.
+  int dev = 0, nsm = 0, coop = 0, per_sm = 0;
+  if (!a->cu_seqlens && a->seqlen > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::NT, Cfg::SMEM) == cudaSuccess &&
+      per_sm >= 1) {
+    const int grid = nsm * per_sm;
+    const int64_t nch = (a->seqlen + Q - 1) / Q, total = (int64_t)units * nch;
+    const int64_t range = (total + grid - 1) / grid;
+    if (units > grid && total / grid >= nch && range <= (int64_t)(kMaxSeg - 2) * nch) {
+      const size_t nslot = (size_t)grid + 1;
+      const size_t off_xh = align_up((int)(nslot * 4), 256);
+      const size_t off_xB = off_xh + nslot * (size_t)(N / 2) * 64 * 2 * 4;
+      const size_t off_xx = off_xB + (size_t)align_up((int)(nslot * R * N * 2), 256);
+      const size_t bytes = off_xx + nslot * (size_t)R * 64 * 2;
+      void* buf = nullptr;
+      cudaMemPool_t pool = handover_pool(dev);
+      if (pool && cudaMallocFromPoolAsync(&buf, bytes, pool, s) == cudaSuccess) {
+        uint8_t* b8 = static_cast<uint8_t*>(buf);
+        p.bal_grid = grid;
+        p.bal_units = units;
+        p.xflag = reinterpret_cast<int*>(b8);
+        p.xh = reinterpret_cast<float*>(b8 + off_xh);
+        p.xB = reinterpret_cast<__nv_bfloat16*>(b8 + off_xB);
+        p.xx = reinterpret_cast<__nv_bfloat16*>(b8 + off_xx);
+        cudaError_t e = cudaMemsetAsync(p.xflag, 0, nslot * 4, s);
+        if (e == cudaSuccess) {
+          void* args[] = {&mx, &mB, &mC, &mth, &p};
+          e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::NT), args,
+                                          Cfg::SMEM, s);
+        }
+        const cudaError_t ef = cudaFreeAsync(buf, s);
+        return (e == cudaSuccess && ef == cudaSuccess) ? M3_OK : M3_ERR_CUDA;
+      }
+      cudaGetLastError();  // no pool memory: the one-CTA-per-unit launch below
+    }
+  }
   kern<<<units, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
   return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }

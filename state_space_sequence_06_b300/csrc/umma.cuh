@@ -142,6 +142,17 @@ __device__ __forceinline__ void mbar_init_fence() {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
+// One arrival per active lane of the calling warp, made by its lowest
+// active lane after the others' preceding shared-memory writes (ordered by
+// the warp barrier): far fewer arrive operations than one per thread.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  const uint32_t mask = __activemask();
+  __syncwarp(mask);
+  if ((threadIdx.x & 31) == (uint32_t)(__ffs(mask) - 1))
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"((uint32_t)__popc(mask))
+                 : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                "r"(bytes)

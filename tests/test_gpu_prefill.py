@@ -220,6 +220,30 @@ def test_full_size_every_output(name):
     st.free()
 
 
+@pytest.mark.parametrize("shape", [dict(dstate=128, rank=1, chunk=64), dict(dstate=64, rank=4, chunk=16),
+                                   dict(dstate=128, rank=1, chunk=64, real=True, euler=True)],
+                         ids=["siso", "mimo4", "mamba2"])
+def test_balanced_schedule_with_state(shape):
+    """More units than SMs (5 x 32 heads, L 600 with a ragged last chunk):
+    the chunked kernel cuts units between CTAs and hands state and carry
+    over; with an initial state and carry, every output, the final state
+    and the carry against the oracle."""
+    wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=5, seqlen=600, nheads=32, h0_std=0.3,
+                      carry=True, dt_shift=-3.0, **shape)
+    inp = synth.prefill_inputs(wl)
+    st = state_for(dims_of(wl), inp["h0"], inp["prev_B"], inp["prev_x"])
+    y = prefill_gpu(inp, wl, state=st)
+    assert m3.m3_device_status() == m3.M3_OK
+    yo, ho, pBo, pxo, _ = oracle.prefill(inp, **oracle_kw(wl), h0=inp["h0"], prev_B=inp["prev_B"],
+                                         prev_x=inp["prev_x"])
+    assert_close(y.cpu().numpy(), yo, TOL["bf16"], "balanced y")
+    h, pB, px = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL["bf16"], "balanced h_final")
+    assert np.array_equal(to_np(pB).reshape(pBo.shape), pBo)
+    assert np.array_equal(to_np(px).reshape(pxo.shape), pxo)
+    st.free()
+
+
 CHUNKED_SHAPES = [(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)]
 
 
