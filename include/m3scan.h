@@ -64,7 +64,8 @@ typedef enum m3_status {
   M3_ERR_UNSUPPORTED = 2, /* a valid request this build has no kernel for (shape, dtype)    */
   M3_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                   */
   M3_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (read by m3_device_status) */
-  M3_ERR_ALLOC = 5        /* device memory allocation failed                               */
+  M3_ERR_ALLOC = 5,       /* device memory allocation failed                               */
+  M3_ERR_SCRATCH = 6      /* m3_scan_prefill_noalloc: the request needs more than its fixed scratch */
 } m3_status;
 
 typedef enum m3_dtype { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
@@ -156,6 +157,30 @@ M3_API m3_status m3_state_view(const m3_state* st, m3_state_ptrs* out);
  * or dtype without a chunked kernel), M3_ERR_CUDA.
  */
 M3_API m3_status m3_scan_prefill(const m3_prefill_args* args, m3_state* st, void* stream);
+
+/*
+ * The same prefill without any device-memory allocation in the call.  The
+ * pages describe no such entry point: it exists for callers that must not
+ * allocate while they run -- for example a serving engine that reserves all
+ * device memory up front, or code whose device memory is planned in
+ * advance.  m3_scan_prefill takes a few MB of stream-ordered pool memory for
+ * the handover slots of its balanced schedule (used when a call has more
+ * (sequence, head) units than the GPU has SMs); this entry point uses a
+ * fixed buffer of M3_NOALLOC_SCRATCH_BYTES that is part of the library's
+ * module memory instead, and calls no allocating routine.
+ *   - The first call on each device looks the buffer's address up (with that
+ *     device current) and can fail with M3_ERR_CUDA; make that first call
+ *     before any stream capture.
+ *   - A request that needs more scratch than the buffer holds returns
+ *     M3_ERR_SCRATCH and enqueues nothing.  The need is about 33 KB per SM at
+ *     N = 128, P = 64 (the buffer covers up to 240 SMs there).
+ *   - The buffer is shared by every call on a device: calls that overlap in
+ *     time (different streams without ordering between them, or different
+ *     host threads) race on it.  Order such calls.
+ * Arguments, results and the other errors are those of m3_scan_prefill.
+ */
+#define M3_NOALLOC_SCRATCH_BYTES (8u << 20)
+M3_API m3_status m3_scan_prefill_noalloc(const m3_prefill_args* args, m3_state* st, void* stream);
 
 /*
  * Decode step: advance every sequence of st by one token, write y, and

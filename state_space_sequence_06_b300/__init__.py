@@ -16,7 +16,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libm3scan.so")
 
-M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_ERR_ALLOC = range(6)
+M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_ERR_ALLOC, M3_ERR_SCRATCH = range(7)
 M3_F32, M3_BF16 = 0, 1
 M3_ALGO_AUTO, M3_ALGO_RECURRENT, M3_ALGO_CHUNKED = 0, 1, 2
 
@@ -68,10 +68,11 @@ def load_library(path: str = LIB_PATH):
     lib.m3_state_free.argtypes = [vp]
     lib.m3_state_view.argtypes = [vp, ctypes.POINTER(m3_state_ptrs)]
     lib.m3_scan_prefill.argtypes = [ctypes.POINTER(m3_prefill_args), vp, vp]
+    lib.m3_scan_prefill_noalloc.argtypes = [ctypes.POINTER(m3_prefill_args), vp, vp]
     lib.m3_decode_step.argtypes = [ctypes.POINTER(m3_decode_args), vp, vp]
     lib.m3_device_status.argtypes = [vp]
     for f in ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
-              "m3_decode_step", "m3_device_status"):
+              "m3_scan_prefill_noalloc", "m3_decode_step", "m3_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.m3_status_string.argtypes = [ctypes.c_int]
     lib.m3_status_string.restype = ctypes.c_char_p
@@ -172,7 +173,7 @@ def m3_state_view(state: State) -> m3_state_ptrs:
 
 
 def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
-                    cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None):
+                    cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None, _entry="m3_scan_prefill"):
     """Prefill.  x [b][L][H][R][P], B/C [b][L][H][R][N], dt/lam [b][L][H],
     theta [b][L][H][N/2] (all bf16 or all f32; lam None: lam = 1, theta
     None: theta = 0), A/D [H] f32, y [b][L][H][R][P]
@@ -188,8 +189,17 @@ def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = N
     if cu_seqlens is not None:
         a.cu_seqlens = _ptr(cu_seqlens)
         a.nseq = cu_seqlens.numel() - 1
-    _check(load_library().m3_scan_prefill(ctypes.byref(a), state.handle if state else None,
-                                          _stream(stream)), "m3_scan_prefill")
+    _check(getattr(load_library(), _entry)(ctypes.byref(a), state.handle if state else None, _stream(stream)),
+           _entry)
+
+
+def m3_scan_prefill_noalloc(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
+                            cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None):
+    """m3_scan_prefill without device-memory allocation in the call: its
+    scratch is a fixed buffer in the library (calls that overlap in time
+    race on it; M3_ERR_SCRATCH when a request needs more)."""
+    m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, state=state, cu_seqlens=cu_seqlens, chunk=chunk,
+                    algo=algo, stream=stream, _entry="m3_scan_prefill_noalloc")
 
 
 def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None):

@@ -1130,8 +1130,11 @@ inline cudaMemPool_t handover_pool(int dev) {
   return pools[dev];
 }
 
+// fixed: caller-provided scratch (fixed_bytes long) for the handover slots
+// instead of the pool; a request that needs more is refused.
 template <int N, int R, int Q, bool RE>
-m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq, cudaStream_t s) {
+m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq, cudaStream_t s,
+                         void* fixed, size_t fixed_bytes) {
   using Cfg = ChunkCfg<N, R, Q, RE>;
   const int H = a->dims.nheads;
   const uint64_t T = (uint64_t)a->seqlen * (a->cu_seqlens ? 1 : a->dims.batch);
@@ -1183,8 +1186,10 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
       const size_t off_xx = off_xB + (size_t)align_up((int)(nslot * R * N * 2), 256);
       const size_t bytes = off_xx + nslot * (size_t)R * 64 * 2;
       void* buf = nullptr;
-      cudaMemPool_t pool = handover_pool(dev);
-      if (pool && cudaMallocFromPoolAsync(&buf, bytes, pool, s) == cudaSuccess) {
+      if (fixed && bytes > fixed_bytes) return M3_ERR_SCRATCH;
+      cudaMemPool_t pool = fixed ? nullptr : handover_pool(dev);
+      if (fixed) buf = fixed;
+      if (fixed || (pool && cudaMallocFromPoolAsync(&buf, bytes, pool, s) == cudaSuccess)) {
         uint8_t* b8 = static_cast<uint8_t*>(buf);
         p.bal_grid = grid;
         p.bal_units = units;
@@ -1198,7 +1203,7 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
           e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(Cfg::NT), args,
                                           Cfg::SMEM, s);
         }
-        const cudaError_t ef = cudaFreeAsync(buf, s);
+        const cudaError_t ef = fixed ? cudaSuccess : cudaFreeAsync(buf, s);
         return (e == cudaSuccess && ef == cudaSuccess) ? M3_OK : M3_ERR_CUDA;
       }
       cudaGetLastError();  // no pool memory: the one-CTA-per-unit launch below
@@ -1212,16 +1217,18 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
 // {(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)}; with
 // theta = 0 (NULL) in {(128, 1, 64), (64, 1, 64), (64, 4, 16)}.
 inline m3_status chunked_prefill(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, void* fixed = nullptr, size_t fixed_bytes = 0) {
   const m3_dims& d = a->dims;
   if (d.in_dtype != M3_BF16 || d.headdim != 64) return M3_ERR_UNSUPPORTED;
   const int R = d.rank, N = d.dstate;
   const int Q = a->chunk > 0 ? a->chunk : (R == 1 ? 64 : 64 / R);
   const bool re = a->theta == nullptr;
 #define M3_CH(NN, RR, QQ) \
-  if (!re && N == NN && R == RR && Q == QQ) return chunked_launch<NN, RR, QQ, false>(a, h, prev_B, prev_x, nseq, s);
+  if (!re && N == NN && R == RR && Q == QQ)                                                  \
+    return chunked_launch<NN, RR, QQ, false>(a, h, prev_B, prev_x, nseq, s, fixed, fixed_bytes);
 #define M3_CH_RE(NN, RR, QQ) \
-  if (re && N == NN && R == RR && Q == QQ) return chunked_launch<NN, RR, QQ, true>(a, h, prev_B, prev_x, nseq, s);
+  if (re && N == NN && R == RR && Q == QQ)                                                   \
+    return chunked_launch<NN, RR, QQ, true>(a, h, prev_B, prev_x, nseq, s, fixed, fixed_bytes);
   M3_CH_RE(128, 1, 64)
   M3_CH_RE(64, 1, 64)
   M3_CH_RE(64, 4, 16)

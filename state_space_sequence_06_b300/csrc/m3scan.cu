@@ -166,6 +166,8 @@ const char* m3_status_string(m3_status s) {
     case M3_ERR_CUDA: return "CUDA error";
     case M3_ERR_TIMEOUT: return "device wait timed out";
     case M3_ERR_ALLOC: return "device allocation failed";
+    case M3_ERR_SCRATCH:
+      return "the request needs more scratch than the fixed buffer of m3_scan_prefill_noalloc holds";
   }
   return "unknown status";
 }
@@ -242,7 +244,13 @@ m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
                                      : decode_launch<float>(p, units, s);
 }
 
-m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The prefill of both entry points; `fixed` (fixed_bytes long) replaces the
+// pool memory of the balanced schedule's handover slots when given.
+m3_status prefill_impl(const m3_prefill_args* a, m3_state* st, void* stream, void* fixed, size_t fixed_bytes) {
   if (!a || !dims_ok(&a->dims) || a->seqlen < 0) return M3_ERR_INVALID_ARG;
   // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
   if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
@@ -265,7 +273,7 @@ m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) 
 
   if (a->algo != M3_ALGO_RECURRENT) {
     m3_status rc = m3::chunked_prefill(a, st ? st->h : nullptr, st ? st->prev_B : nullptr,
-                                       st ? st->prev_x : nullptr, nseq, s);
+                                       st ? st->prev_x : nullptr, nseq, s, fixed, fixed_bytes);
     if (rc != M3_ERR_UNSUPPORTED || a->algo == M3_ALGO_CHUNKED) return rc;
   }
   m3::RecurrentParams p{};
@@ -278,6 +286,31 @@ m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) 
   p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
   return bf16 ? recurrent_launch<__nv_bfloat16>(p, a->dims.rank, units, s)
               : recurrent_launch<float>(p, a->dims.rank, units, s);
+}
+
+// The fixed scratch of m3_scan_prefill_noalloc: module memory, reserved when
+// the library is loaded, never allocated by a call.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[M3_NOALLOC_SCRATCH_BYTES];
+
+}  // namespace
+
+extern "C" {
+
+m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) {
+  return prefill_impl(a, st, stream, nullptr, 0);
+}
+
+m3_status m3_scan_prefill_noalloc(const m3_prefill_args* a, m3_state* st, void* stream) {
+  // the scratch's address on the current device, looked up once per device
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return M3_ERR_CUDA;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return M3_ERR_CUDA;
+    addr[dev] = p;
+  }
+  return prefill_impl(a, st, stream, addr[dev], M3_NOALLOC_SCRATCH_BYTES);
 }
 
 m3_status m3_device_status(void* stream) {
