@@ -1077,6 +1077,14 @@ inline PFN_encodeTiled get_encode_tiled() {
 }
 
 // 3-D bf16 tensor [T][H][inner] (inner contiguous), box [Q][1][inner], unswizzled.
+// L2 fills no wider than one (token, head) row: a wider promotion pulls in
+// the neighbouring head's row, which a balanced schedule reaches much later
+// (after the line has left L2), so it would be read from HBM twice.
+inline CUtensorMapL2promotion row_promotion(uint64_t row_bytes) {
+  return row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                          : (row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
+}
+
 inline bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H, uint64_t T, uint32_t Q) {
   PFN_encodeTiled enc = get_encode_tiled();
   if (!enc) return false;
@@ -1085,7 +1093,7 @@ inline bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64
   cuuint32_t box[3] = {(cuuint32_t)inner, 1, Q};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, row_promotion(inner * 2),
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1101,7 +1109,7 @@ inline bool make_map_4d_sw128(CUtensorMap* m, const void* base, uint64_t inner, 
   cuuint32_t box[4] = {64, (cuuint32_t)R, 1, Q};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, row_promotion(inner * R * 2),
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
