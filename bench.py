@@ -46,12 +46,13 @@ def workload_bytes(wl) -> dict:
     the f32 state read (when it carries in) and written once."""
     isz = 2 if wl.dtype == "bf16" else 4
     H, P, N, R = wl.nheads, wl.headdim, wl.dstate, wl.rank
-    # per token and head: x, B, C, dt, and lam / theta unless they are the
-    # special values (not read at all then)
-    per_in = R * P + 2 * R * N + 1 + (0 if wl.euler else 1) + (0 if wl.real else N // 2)
+    G = wl.groups
+    # per token and head: x, dt, and lam / theta unless they are the special
+    # values (not read at all then); B and C once per group of heads
+    per_in = R * P + 1 + (0 if wl.euler else 1) + (0 if wl.real else N // 2) + 2 * R * N * G / H
     if wl.kind == "decode":
         units = wl.batch * H
-        per_step_in = units * per_in * isz
+        per_step_in = int(round(units * per_in * isz))
         carry = units * (R * N + R * P) * isz * 2  # read old, write new
         state = units * N * P * 4 * 2
         y = units * R * P * 4
@@ -63,8 +64,8 @@ def workload_bytes(wl) -> dict:
     nseq = wl.nseq if wl.kind == "varlen" else wl.batch
     state = nseq * H * N * P * 4 * 2  # h0 read + h_final write
     carry = nseq * H * (R * N + R * P) * isz * 2
-    total = th * (per_th_in + R * P * 4) + state + carry
-    return dict(per_unit_of_work=total, unit="pass", inputs=th * per_th_in, y=th * R * P * 4,
+    total = int(round(th * (per_th_in + R * P * 4))) + state + carry
+    return dict(per_unit_of_work=total, unit="pass", inputs=int(round(th * per_th_in)), y=th * R * P * 4,
                 state=state, carry=carry, per_token_head=per_th_in + R * P * 4)
 
 
@@ -266,6 +267,8 @@ def config_of(wl):
         c["chunk"] = wl.chunk
     if wl.kind == "varlen":
         c["nseq"] = wl.nseq
+    if wl.ngroups:
+        c["ngroups"] = wl.ngroups
     if wl.real or wl.euler:
         c["special_case"] = "Mamba-2: " + ", ".join(
             ([("theta = 0 (real state)")] if wl.real else []) + (["lam = 1 (first order)"] if wl.euler else []))
@@ -455,8 +458,8 @@ def main():
     others = []
     if not args.quick:
         for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "siso_n64_b8_l4096", "mamba2_b8_l4096",
-                     "decode_siso_b256", "decode_mimo4_b256", "decode_siso_n64_b256", "decode_mamba2_b256",
-                     "tiny_f32"):
+                     "siso_g1_b8_l4096", "mimo4_g1_b8_l4096", "decode_siso_b256", "decode_mimo4_b256",
+                     "decode_siso_n64_b256", "decode_mamba2_b256", "decode_siso_g1_b256", "tiny_f32"):
             if name == args.workload:
                 continue
             sargs = argparse.Namespace(**vars(args))
@@ -532,6 +535,8 @@ def sampled_parity(wl, m3, t, y, st, cu, algo):
 def measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world):
     """The same metric through the public API from pinned host buffers: each
     step copies its inputs host -> device, runs the scan and copies y back."""
+    if wl.kind == "decode":
+        return measure_e2e_decode(wl, m3, torch, t, st, args, world)
     keys = tuple(k for k in ("x", "B", "C", "dt", "lam", "theta") if t[k] is not None)
     host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in keys}
     for k in keys:
@@ -559,6 +564,43 @@ def measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world):
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
     return {"value": units * steps * world / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+
+def measure_e2e_decode(wl, m3, torch, t, st, args, world):
+    """Decode end to end: each pass copies the inputs of its T tokens from
+    pinned host memory, runs T decode steps (each writing its own slice of
+    a [T][b][H][R][P] output) and copies every step's y back."""
+    keys = tuple(k for k in ("x", "B", "C", "dt", "lam", "theta") if t[k] is not None)
+    host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in keys}
+    for k in keys:
+        host[k].copy_(t[k])
+    T = t["x"].shape[0]
+    y_all = torch.empty(t["x"].shape, dtype=torch.float32, device="cuda")
+    yh = torch.empty(y_all.shape, dtype=torch.float32, pin_memory=True)
+    torch.cuda.synchronize()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = y_all.numel() * 4
+
+    def one():
+        for k in keys:
+            t[k].copy_(host[k], non_blocking=True)
+        lam, th = t["lam"], t["theta"]
+        for i in range(T):
+            m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], None if lam is None else lam[i],
+                              None if th is None else th[i], t["A"], t["D"], y_all[i], st)
+        yh.copy_(y_all, non_blocking=True)
+
+    steps = max(2, min(args.steps, 3))
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    return {"value": T * steps * world / el, "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
 
 

@@ -115,6 +115,11 @@ typedef struct m3_prefill_args {
   const int32_t* cu_seqlens; /* device [nseq+1], nondecreasing, cu[0] = 0, cu[nseq] = L; or NULL */
   int32_t nseq;              /* sequences in the packed batch (ignored without cu_seqlens) */
   float* y;                  /* [batch][L][H][R][P] f32 output */
+  int32_t ngroups; /* G: B and C shared by groups of H/G consecutive heads, laid out
+                      [batch][L][G][R][N] (head h uses group h / (H / G)); must divide H;
+                      0 (or H) = one B and C per head, [batch][L][H][R][N].  The pages
+                      give B and C per head; groups are an addressing variant only (the
+                      recurrence of each head is unchanged) */
 } m3_prefill_args;
 
 /* One decode step: a single new token per sequence. */
@@ -129,6 +134,7 @@ typedef struct m3_decode_args {
   const float* A;    /* [H] f32 */
   const float* D;    /* [H] f32 */
   float* y;          /* [batch][H][R][P] f32 output */
+  int32_t ngroups;   /* as in m3_prefill_args: B and C [batch][G][R][N]; 0 = per head */
 } m3_decode_args;
 
 /*

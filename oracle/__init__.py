@@ -103,7 +103,8 @@ def prefill(inp: dict, *, batch, L, H, P, N, R, dtype, cu_seqlens=None, units=No
             h0=None, prev_B=None, prev_x=None, nthreads=None, lib=None):
     """Run the oracle over a prefill workload (or a subset of its units).
 
-    ``inp`` holds x [b][L][H][R][P], B/C [b][L][H][R][N], dt/lam [b][L][H],
+    ``inp`` holds x [b][L][H][R][P], B/C [b][L][G][R][N] (G groups of
+    consecutive heads share B and C; G = H: one per head), dt/lam [b][L][H],
     theta [b][L][H][N/2], A/D [H].  Units are ``s*H + h`` where s is the
     batch row, or the sequence index when ``cu_seqlens`` is given (then
     b == 1).  ``h0``/``prev_B``/``prev_x`` are per-sequence initial states
@@ -117,6 +118,7 @@ def prefill(inp: dict, *, batch, L, H, P, N, R, dtype, cu_seqlens=None, units=No
     all_units = list(range(nseq * H))
     sel = all_units if units is None else list(units)
     K = N // 2
+    G = np.shape(inp["B"])[2]
     tab, spans, yoff = [], [], 0
     for u in sel:
         s, hd = divmod(u, H)
@@ -128,7 +130,7 @@ def prefill(inp: dict, *, batch, L, H, P, N, R, dtype, cu_seqlens=None, units=No
         tab.append(dict(
             ntok=ntok,
             x0=(tok0 * H + hd) * R * P, xs=H * R * P,
-            b0=(tok0 * H + hd) * R * N, bs=H * R * N,
+            b0=(tok0 * G + hd // (H // G)) * R * N, bs=G * R * N,
             s0=tok0 * H + hd, ss=H,
             q0=(tok0 * H + hd) * K, qs=H * K,
             y0=yoff, ys=R * P, head=hd,
@@ -163,12 +165,13 @@ def prefill(inp: dict, *, batch, L, H, P, N, R, dtype, cu_seqlens=None, units=No
 def decode(inp: dict, *, batch, H, P, N, R, dtype, steps, units=None, nthreads=None, lib=None):
     """Run ``steps`` single-token decode steps from the initial state in ``inp``.
 
-    ``inp`` holds per-step tensors x [T][b][H][R][P], B/C [T][b][H][R][N],
+    ``inp`` holds per-step tensors x [T][b][H][R][P], B/C [T][b][G][R][N],
     dt/lam [T][b][H], theta [T][b][H][N/2] plus h0, prev_B, prev_x.  Units
     are ``b*H + h``.  Returns ``(y, h, prev_B, prev_x)`` with y
     [T][b][H][R][P] when every unit is walked, else a dict unit -> [T][R][P].
     """
     K = N // 2
+    G = np.shape(inp["B"])[2]  # B/C [T][b][G][R][N]
     sel = list(range(batch * H)) if units is None else list(units)
     tab = []
     for i, u in enumerate(sel):
@@ -176,7 +179,7 @@ def decode(inp: dict, *, batch, H, P, N, R, dtype, steps, units=None, nthreads=N
         tab.append(dict(
             ntok=steps,
             x0=u * R * P, xs=batch * H * R * P,
-            b0=u * R * N, bs=batch * H * R * N,
+            b0=(b * G + hd // (H // G)) * R * N, bs=batch * G * R * N,
             s0=u, ss=batch * H,
             q0=u * K, qs=batch * H * K,
             y0=i * steps * R * P, ys=R * P, head=hd,

@@ -44,12 +44,13 @@ class m3_prefill_args(ctypes.Structure):
     _fields_ = [("dims", m3_dims), ("seqlen", ctypes.c_int64), ("chunk", ctypes.c_int32),
                 ("algo", ctypes.c_int32)] + \
         [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "cu_seqlens")] + \
-        [("nseq", ctypes.c_int32), ("y", ctypes.c_void_p)]
+        [("nseq", ctypes.c_int32), ("y", ctypes.c_void_p), ("ngroups", ctypes.c_int32)]
 
 
 class m3_decode_args(ctypes.Structure):
     _fields_ = [("dims", m3_dims)] + \
-        [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "y")]
+        [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "y")] + \
+        [("ngroups", ctypes.c_int32)]
 
 
 _lib = None
@@ -174,8 +175,8 @@ def m3_state_view(state: State) -> m3_state_ptrs:
 
 def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
                     cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None, _entry="m3_scan_prefill"):
-    """Prefill.  x [b][L][H][R][P], B/C [b][L][H][R][N], dt/lam [b][L][H],
-    theta [b][L][H][N/2] (all bf16 or all f32; lam None: lam = 1, theta
+    """Prefill.  x [b][L][H][R][P], B/C [b][L][G][R][N] (G groups of heads;
+    G = H: one per head), dt/lam [b][L][H], theta [b][L][H][N/2] (all bf16 or all f32; lam None: lam = 1, theta
     None: theta = 0), A/D [H] f32, y [b][L][H][R][P]
     f32 (written).  ``cu_seqlens`` (int32 CUDA tensor) packs sequences in a
     batch of one row."""
@@ -183,6 +184,7 @@ def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = N
     N = B.shape[-1]
     a = m3_prefill_args()
     a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
+    a.ngroups = B.shape[2]  # B and C [b][L][G][R][N]: G = H is one per head
     a.seqlen, a.chunk, a.algo = L, chunk, algo
     a.x, a.B, a.C, a.dt, a.lam, a.theta = (_ptr(t) for t in (x, B, C, dt, lam, theta))
     a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
@@ -203,13 +205,14 @@ def m3_scan_prefill_noalloc(x, B, C, dt, lam, theta, A, D, y, *, state: State | 
 
 
 def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None):
-    """One decode step.  x [b][H][R][P], B/C [b][H][R][N], dt/lam [b][H],
-    theta [b][H][N/2] (lam / theta None: 1 / 0), A/D [H] f32, y [b][H][R][P]
+    """One decode step.  x [b][H][R][P], B/C [b][G][R][N] (G groups of heads;
+    G = H: one per head), dt/lam [b][H], theta [b][H][N/2] (lam / theta None: 1 / 0), A/D [H] f32, y [b][H][R][P]
     f32 (written)."""
     b, H, R, P = x.shape
     N = B.shape[-1]
     a = m3_decode_args()
     a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
+    a.ngroups = B.shape[1]
     a.x, a.B, a.C, a.dt, a.lam, a.theta = (_ptr(t) for t in (x, B, C, dt, lam, theta))
     a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
     _check(load_library().m3_decode_step(ctypes.byref(a), state.handle, _stream(stream)),

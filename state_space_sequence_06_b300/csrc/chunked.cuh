@@ -63,6 +63,7 @@ struct ChunkParams {
   __nv_bfloat16* prev_x;
   int64_t L;
   int H;
+  int G;  // B and C groups (head h uses group h / (H / G))
   // Balanced schedule (bal_grid == 0: one CTA per (sequence, head) unit).
   // With fixed-length sequences the bal_units units' chunks, unit after
   // unit, are cut into bal_grid equal ranges, one per CTA (all resident at
@@ -729,7 +730,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       }
       if (cB) {
         const int64_t last = (sSegTok0[si] + seg_ntok(si) - 1) * H + head;
-        for (int i = tt; i < R * N; i += NSTA) cB[i] = p.B[last * R * N + i];
+        const int64_t lastg = (sSegTok0[si] + seg_ntok(si) - 1) * p.G + head / (H / p.G);
+        for (int i = tt; i < R * N; i += NSTA) cB[i] = p.B[lastg * R * N + i];
         for (int i = tt; i < R * P; i += NSTA) cx[i] = p.x[last * R * P + i];
       }
       if (to_slot) {
@@ -1002,6 +1004,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // ======================= TMA warp (one thread issues)
     if (lane == 0) {
       int issued0 = 0, issued1 = 0;
+      const int hpg = H / p.G;  // heads per B / C group
       auto issue = [&](int c) {
         const int s = c & 1;
         uint8_t* stg = stage(s);
@@ -1012,8 +1015,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         tma_load_4d(saddr(stg + Cfg::OFF_X), &tm_x, bar, 0, 0, head, t);
 #pragma unroll
         for (int kb = 0; kb < N / 64; ++kb) {
-          tma_load_4d(saddr(stg + Cfg::OFF_B + kb * Cfg::BB), &tm_B, bar, 64 * kb, 0, head, t);
-          tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head, t);
+          tma_load_4d(saddr(stg + Cfg::OFF_B + kb * Cfg::BB), &tm_B, bar, 64 * kb, 0, head / hpg, t);
+          tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head / hpg, t);
         }
         if (!RE) tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
         if (s) ++issued1; else ++issued0;
@@ -1027,8 +1030,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         tma_prefetch_4d(&tm_x, 0, 0, head, t);
 #pragma unroll
         for (int kb = 0; kb < N / 64; ++kb) {
-          tma_prefetch_4d(&tm_B, 64 * kb, 0, head, t);
-          tma_prefetch_4d(&tm_C, 64 * kb, 0, head, t);
+          tma_prefetch_4d(&tm_B, 64 * kb, 0, head / hpg, t);
+          tma_prefetch_4d(&tm_C, 64 * kb, 0, head / hpg, t);
         }
         if (!RE) tma_prefetch_3d(&tm_th, 0, head, t);
       };
@@ -1147,8 +1150,9 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   const int H = a->dims.nheads;
   const uint64_t T = (uint64_t)a->seqlen * (a->cu_seqlens ? 1 : a->dims.batch);
   CUtensorMap mx, mB, mC, mth;
-  if (!make_map_4d_sw128(&mx, a->x, 64, R, H, T, Q) || !make_map_4d_sw128(&mB, a->B, N, R, H, T, Q) ||
-      !make_map_4d_sw128(&mC, a->C, N, R, H, T, Q))
+  const int G = a->ngroups > 0 ? a->ngroups : H;
+  if (!make_map_4d_sw128(&mx, a->x, 64, R, H, T, Q) || !make_map_4d_sw128(&mB, a->B, N, R, G, T, Q) ||
+      !make_map_4d_sw128(&mC, a->C, N, R, G, T, Q))
     return M3_ERR_CUDA;
   if (RE) {
     mth = mx;  // not read: theta = 0
@@ -1169,6 +1173,7 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   p.prev_x = static_cast<__nv_bfloat16*>(prev_x);
   p.L = a->seqlen;
   p.H = H;
+  p.G = G;
   auto kern = chunked_prefill_kernel<N, R, Q, RE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;

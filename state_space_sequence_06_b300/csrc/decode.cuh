@@ -37,6 +37,7 @@ struct DecodeParams {
   void* prev_B;
   void* prev_x;
   int H, P, N, R;
+  int G;   // B and C groups (head h uses group h / (H / G))
   int K;   // N / 2
   int PP;  // P / 2
   int KG;  // k groups (blockDim.x / PP)
@@ -83,8 +84,9 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
   const uint32_t state_bytes = (uint32_t)K * PP * 16;
 
   const T* xg = static_cast<const T*>(p.x) + (int64_t)unit * R * P;
-  const T* Bg = static_cast<const T*>(p.B) + (int64_t)unit * R * N;
-  const T* Cg = static_cast<const T*>(p.C) + (int64_t)unit * R * N;
+  const int64_t brow = (int64_t)(unit / p.H) * p.G + head / (p.H / p.G);  // this unit's B / C row
+  const T* Bg = static_cast<const T*>(p.B) + brow * R * N;
+  const T* Cg = static_cast<const T*>(p.C) + brow * R * N;
   T* pBg = static_cast<T*>(p.prev_B) + (int64_t)unit * R * N;
   T* pxg = static_cast<T*>(p.prev_x) + (int64_t)unit * R * P;
   const T* thg = p.theta ? static_cast<const T*>(p.theta) + (int64_t)unit * K : nullptr;

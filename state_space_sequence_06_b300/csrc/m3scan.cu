@@ -230,6 +230,7 @@ m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
   if (!a || !st || !dims_ok(&a->dims) || !same_dims(a->dims, st->dims)) return M3_ERR_INVALID_ARG;
   // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
   if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
+  if (a->ngroups < 0 || (a->ngroups > 0 && a->dims.nheads % a->ngroups != 0)) return M3_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
       !aligned16(a->y))
     return M3_ERR_INVALID_ARG;
@@ -238,6 +239,7 @@ m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
   p.A = a->A; p.D = a->D; p.y = a->y;
   p.h = st->h; p.prev_B = st->prev_B; p.prev_x = st->prev_x;
   p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
+  p.G = a->ngroups > 0 ? a->ngroups : a->dims.nheads;
   const int units = a->dims.batch * a->dims.nheads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return a->dims.in_dtype == M3_BF16 ? decode_launch<__nv_bfloat16>(p, units, s)
@@ -254,6 +256,7 @@ m3_status prefill_impl(const m3_prefill_args* a, m3_state* st, void* stream, voi
   if (!a || !dims_ok(&a->dims) || a->seqlen < 0) return M3_ERR_INVALID_ARG;
   // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
   if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
+  if (a->ngroups < 0 || (a->ngroups > 0 && a->dims.nheads % a->ngroups != 0)) return M3_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
       !aligned16(a->y))
     return M3_ERR_INVALID_ARG;
@@ -284,6 +287,7 @@ m3_status prefill_impl(const m3_prefill_args* a, m3_state* st, void* stream, voi
   p.prev_x = st ? st->prev_x : nullptr;
   p.L = a->seqlen;
   p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
+  p.G = a->ngroups > 0 ? a->ngroups : a->dims.nheads;
   return bf16 ? recurrent_launch<__nv_bfloat16>(p, a->dims.rank, units, s)
               : recurrent_launch<float>(p, a->dims.rank, units, s);
 }

@@ -35,6 +35,7 @@ struct RecurrentParams {
   void* prev_x;
   int64_t L;      // tokens per row (total with cu_seqlens)
   int H, P, N, K, R;
+  int G;          // B and C groups (head h uses group h / (H / G))
   int KS;         // threads per p (power of two <= 32)
   int TB;         // tokens staged per block
 };
@@ -98,7 +99,7 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
     __syncthreads();  // previous block fully consumed (row 0 already moved)
     for (int i = tid; i < nb * RN; i += blockDim.x) {
       const int tb = i / RN, e = i % RN;
-      const int64_t g = ((tok0 + t0 + tb) * H + head) * RN + e;
+      const int64_t g = ((tok0 + t0 + tb) * p.G + head / (H / p.G)) * RN + e;
       Bs[(tb + 1) * RN + e] = ldf(Bg, g);
       Cs[tb * RN + e] = ldf(Cg, g);
     }
@@ -185,9 +186,10 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
   }
   if (ntok > 0 && p.prev_B) {
     const int64_t last = (tok0 + ntok - 1) * H + head;
+    const int64_t lastg = (tok0 + ntok - 1) * p.G + head / (H / p.G);
     T* pB = static_cast<T*>(p.prev_B) + (int64_t)unit * RN;
     T* px = static_cast<T*>(p.prev_x) + (int64_t)unit * RP;
-    for (int i = tid; i < RN; i += blockDim.x) pB[i] = Bg[last * RN + i];
+    for (int i = tid; i < RN; i += blockDim.x) pB[i] = Bg[lastg * RN + i];
     for (int i = tid; i < RP; i += blockDim.x) px[i] = xg[last * RP + i];
   }
 }

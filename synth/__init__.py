@@ -119,6 +119,7 @@ class Workload:
     seed: int = 0
     real: bool = False   # theta = 0: a real state (given as None)
     euler: bool = False  # lam = 1: first-order exponential Euler (given as None)
+    ngroups: int = 0  # B/C groups shared by nheads/ngroups consecutive heads; 0: one per head
     cu_seqlens: np.ndarray | None = field(default=None, repr=False)
     # shard of a global problem: this shard's `batch` sequences (varlen:
     # `nseq` sequences) are number shard_index*batch.. of a global batch of
@@ -126,6 +127,10 @@ class Workload:
     shard_index: int = 0
     shards: int = 1
     tok_offset: int = 0  # varlen: first global token of this shard
+
+    @property
+    def groups(self) -> int:
+        return self.ngroups or self.nheads
 
     @property
     def units(self) -> int:
@@ -156,6 +161,14 @@ def workloads() -> dict:
         "decode_mamba2_b256": Workload(
             "decode_mamba2_b256", "decode", 256, 1024, 32, 64, 128, 1, "bf16", h0_std=0.1, carry=True,
             real=True, euler=True),
+        # B and C shared by all heads (one group), as a mixer layer usually projects them
+        "siso_g1_b8_l4096": Workload("siso_g1_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16", chunk=64,
+                                     ngroups=1),
+        "mimo4_g1_b8_l4096": Workload("mimo4_g1_b8_l4096", "prefill", 8, 4096, 32, 64, 64, 4, "bf16", chunk=16,
+                                      ngroups=1),
+        "decode_siso_g1_b256": Workload(
+            "decode_siso_g1_b256", "decode", 256, 1024, 32, 64, 128, 1, "bf16", h0_std=0.1, carry=True,
+            ngroups=1),
         "varlen_16": Workload(
             "varlen_16", "varlen", 1, 0, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0,
             nseq=16, len_lo=256, len_hi=8192,
@@ -203,10 +216,12 @@ def prefill_inputs(wl: Workload) -> dict:
     """All tensors of a prefill workload.
 
     Layouts (token-major, heads inside):  x [b][L][H][R][P], B and C
-    [b][L][H][R][N], dt and lam [b][L][H], theta [b][L][H][N/2]; A and D
-    [H] float32.  For a varlen workload b = 1 and L = total tokens.
+    [b][L][G][R][N] (G = ngroups, else H), dt and lam [b][L][H], theta
+    [b][L][H][N/2]; A and D [H] float32.  For a varlen workload b = 1 and
+    L = total tokens.
     """
     b, L, H, P, N, R = wl.batch, wl.seqlen, wl.nheads, wl.headdim, wl.dstate, wl.rank
+    G = wl.groups
     dt_ = wl.dtype
     s = wl.seed
     # first token (over b*L) and first unit of this shard in the global problem
@@ -223,8 +238,8 @@ def prefill_inputs(wl: Workload) -> dict:
 
     d = {
         "x": tok((b, L, H, R, P), S_X, K_NORMAL, 0.0, 1.0),
-        "B": tok((b, L, H, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
-        "C": tok((b, L, H, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "B": tok((b, L, G, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "C": tok((b, L, G, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
         "dt": tok((b, L, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
         "lam": tok((b, L, H), S_LAM, K_SIGMOID, 0.0, 0.0),
         "theta": tok((b, L, H, N // 2), S_THETA, K_UNIFORM, 0.0, np.pi),
@@ -247,7 +262,7 @@ def prefill_inputs(wl: Workload) -> dict:
 def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -> dict:
     """Per-step decode inputs for steps first_step .. first_step+steps.
 
-    Layouts: x [T][b][H][R][P], B and C [T][b][H][R][N], dt and lam
+    Layouts: x [T][b][H][R][P], B and C [T][b][G][R][N], dt and lam
     [T][b][H], theta [T][b][H][N/2]; initial state h0 [b][H][N/2][P][2]
     float32 and the previous-token carry prev_B [b][H][R][N], prev_x
     [b][H][R][P].  Step t is element range t*size.. of each stream, so any
@@ -255,6 +270,7 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
     """
     T = wl.seqlen if steps is None else steps
     b, H, P, N, R = wl.batch, wl.nheads, wl.headdim, wl.dstate, wl.rank
+    G = wl.groups
     dt_ = wl.dtype
     s = wl.seed
 
@@ -278,8 +294,8 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
 
     d = {
         "x": step_fill((b, H, R, P), S_X, K_NORMAL, 0.0, 1.0),
-        "B": step_fill((b, H, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
-        "C": step_fill((b, H, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "B": step_fill((b, G, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "C": step_fill((b, G, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
         "dt": step_fill((b, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
         "lam": step_fill((b, H), S_LAM, K_SIGMOID, 0.0, 0.0),
         "theta": step_fill((b, H, N // 2), S_THETA, K_UNIFORM, 0.0, np.pi),

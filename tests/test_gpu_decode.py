@@ -39,8 +39,11 @@ def run_decode(wl, steps, units=None, window=None):
         for k in ("x", "B", "C", "dt", "lam", "theta"):
             if d[k] is None:  # lam = 1 / theta = 0: the oracle takes None the same way
                 continue
-            v = d[k].reshape((n, b * H) + d[k].shape[3:])[:, sel] if k not in ("dt", "lam") else \
-                d[k].reshape(n, b * H)[:, sel]
+            a = d[k]
+            if k in ("B", "C") and a.shape[2] != H:  # grouped: the oracle below takes one head per row
+                a = np.repeat(a, H // a.shape[2], axis=2)
+            v = a.reshape((n, b * H) + a.shape[3:])[:, sel] if k not in ("dt", "lam") else \
+                a.reshape(n, b * H)[:, sel]
             allin.setdefault(k, []).append(v)
     torch.cuda.synchronize()
     assert m3.m3_device_status() == m3.M3_OK
