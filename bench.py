@@ -45,6 +45,7 @@ def workload_bytes(wl) -> dict:
     """Algorithmic bytes of one pass: every input read once, y written once,
     the f32 state read (when it carries in) and written once."""
     isz = 2 if wl.dtype == "bf16" else 4
+    ysz = 2 if wl.y_bf16 else 4
     H, P, N, R = wl.nheads, wl.headdim, wl.dstate, wl.rank
     G = wl.groups
     # per token and head: x, dt, and lam / theta unless they are the special
@@ -55,7 +56,7 @@ def workload_bytes(wl) -> dict:
         per_step_in = int(round(units * per_in * isz))
         carry = units * (R * N + R * P) * isz * 2  # read old, write new
         state = units * N * P * 4 * 2
-        y = units * R * P * 4
+        y = units * R * P * ysz
         return dict(per_unit_of_work=per_step_in + carry + state + y, unit="step",
                     inputs=per_step_in, state=state, carry=carry, y=y)
     tokens = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
@@ -64,9 +65,9 @@ def workload_bytes(wl) -> dict:
     nseq = wl.nseq if wl.kind == "varlen" else wl.batch
     state = nseq * H * N * P * 4 * 2  # h0 read + h_final write
     carry = nseq * H * (R * N + R * P) * isz * 2
-    total = int(round(th * (per_th_in + R * P * 4))) + state + carry
-    return dict(per_unit_of_work=total, unit="pass", inputs=int(round(th * per_th_in)), y=th * R * P * 4,
-                state=state, carry=carry, per_token_head=per_th_in + R * P * 4)
+    total = int(round(th * (per_th_in + R * P * ysz))) + state + carry
+    return dict(per_unit_of_work=total, unit="pass", inputs=int(round(th * per_th_in)), y=th * R * P * ysz,
+                state=state, carry=carry, per_token_head=per_th_in + R * P * ysz)
 
 
 # the sources each kernel is compiled from (its launcher included)
@@ -269,6 +270,9 @@ def config_of(wl):
         c["nseq"] = wl.nseq
     if wl.ngroups:
         c["ngroups"] = wl.ngroups
+    if wl.prologue:
+        c["prologue"] = "fused: dt = softplus(dt + dt_bias), B and C rows RMS-normalised"
+    c["y_dtype"] = "bf16" if wl.y_bf16 else "f32"
     if wl.real or wl.euler:
         c["special_case"] = "Mamba-2: " + ", ".join(
             ([("theta = 0 (real state)")] if wl.real else []) + (["lam = 1 (first order)"] if wl.euler else []))
@@ -276,6 +280,14 @@ def config_of(wl):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+
+def prologue_kw(wl, m3, t):
+    """Prologue arguments of a scan call: raw-input workloads have the kernel
+    apply softplus(dt + dt_bias) and the RMS norm of B and C rows."""
+    if not wl.prologue:
+        return {}
+    return dict(prologue=m3.M3_PRO_DT_SOFTPLUS | m3.M3_PRO_BC_NORM, dt_bias=t["dt_bias"])
 
 
 def dev_tensor(torch, a):
@@ -306,7 +318,7 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
         st = m3.m3_state_alloc(m3.make_dims(wl.batch, H, P, N, R, dims_dtype))
         hv, pB, px = st.views()
         h0, pB0, px0 = dev_tensor(torch, d["h0"]), dev_tensor(torch, d["prev_B"]), dev_tensor(torch, d["prev_x"])
-        y = torch.empty((wl.batch, H, R, P), dtype=torch.float32, device="cuda")
+        y = torch.empty((wl.batch, H, R, P), dtype=torch.bfloat16 if wl.y_bf16 else torch.float32, device="cuda")
         del d
 
         def step():
@@ -328,18 +340,20 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
     else:
         inp = synth.prefill_inputs(wl)
         t = {k: dev_tensor(torch, inp[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
+        t["dt_bias"] = dev_tensor(torch, inp.get("dt_bias"))
+        pkw = prologue_kw(wl, m3, t)
         nseq = wl.batch
         if wl.kind == "varlen":
             cu = torch.from_numpy(wl.cu_seqlens).cuda()
             nseq = wl.nseq
         st = m3.m3_state_alloc(m3.make_dims(nseq, H, P, N, R, dims_dtype))
-        y = torch.empty(t["x"].shape, dtype=torch.float32, device="cuda")
+        y = torch.empty(t["x"].shape, dtype=torch.bfloat16 if wl.y_bf16 else torch.float32, device="cuda")
 
         def step():
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                               state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk)
+                               state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk, **pkw)
             e1.record(stream)
             ev_pairs.append((e0, e1))
 
@@ -353,7 +367,7 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
         if wl.dtype == "bf16" and algo != m3.M3_ALGO_RECURRENT:
             try:
                 m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                                   state=st, cu_seqlens=cu, algo=m3.M3_ALGO_CHUNKED, chunk=wl.chunk)
+                                   state=st, cu_seqlens=cu, algo=m3.M3_ALGO_CHUNKED, chunk=wl.chunk, **pkw)
                 path_dtype = "f16x2 (hi/lo f16 operands, f32 accumulate)"
             except m3.M3Error as e:
                 if e.status != m3.M3_ERR_UNSUPPORTED:
@@ -458,7 +472,8 @@ def main():
     others = []
     if not args.quick:
         for name in ("mimo4_b8_l4096", "long_l16384", "varlen_16", "siso_n64_b8_l4096", "mamba2_b8_l4096",
-                     "siso_g1_b8_l4096", "mimo4_g1_b8_l4096", "decode_siso_b256", "decode_mimo4_b256",
+                     "siso_g1_b8_l4096", "mimo4_g1_b8_l4096", "siso_ybf16_b8_l4096", "siso_prologue_b8_l4096",
+                     "decode_siso_b256", "decode_mimo4_b256",
                      "decode_siso_n64_b256", "decode_mamba2_b256", "decode_siso_g1_b256", "tiny_f32"):
             if name == args.workload:
                 continue
@@ -516,12 +531,16 @@ def sampled_parity(wl, m3, t, y, st, cu, algo):
     pB.zero_()
     px.zero_()
     m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y, state=st,
-                       cu_seqlens=cu, algo=algo, chunk=wl.chunk)
+                       cu_seqlens=cu, algo=algo, chunk=wl.chunk, **prologue_kw(wl, m3, t))
     torch.cuda.synchronize()
     rms = float(torch.sqrt((y.double() ** 2).mean()).item())
     units = [0, U - 1]
+    dtype = wl.dtype
+    if wl.prologue:
+        inp = oracle.apply_prologue(inp, wl.dtype, dt_softplus=True, bc_norm=True, dt_bias=inp["dt_bias"])
+        dtype = "f64"
     yo, ho, _, _, spans = oracle.prefill(inp, batch=wl.batch, L=wl.seqlen, H=wl.nheads, P=wl.headdim,
-                                         N=wl.dstate, R=wl.rank, dtype=wl.dtype, cu_seqlens=cu_np, units=units)
+                                         N=wl.dstate, R=wl.rank, dtype=dtype, cu_seqlens=cu_np, units=units)
     err = 0.0
     for u, (b, t0, n, hd, _) in zip(units, spans):
         g = y[b, t0:t0 + n, hd].double().cpu().numpy()
@@ -544,14 +563,14 @@ def measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world):
     yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
     torch.cuda.synchronize()
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
-    d2h = y.numel() * 4
+    d2h = y.numel() * y.element_size()
     units = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
 
     def one():
         for k in keys:
             t[k].copy_(host[k], non_blocking=True)
         m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                           state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk)
+                           state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk, **prologue_kw(wl, m3, t))
         yh.copy_(y, non_blocking=True)
 
     steps = max(3, min(args.steps, 10))
@@ -577,11 +596,11 @@ def measure_e2e_decode(wl, m3, torch, t, st, args, world):
     for k in keys:
         host[k].copy_(t[k])
     T = t["x"].shape[0]
-    y_all = torch.empty(t["x"].shape, dtype=torch.float32, device="cuda")
-    yh = torch.empty(y_all.shape, dtype=torch.float32, pin_memory=True)
+    y_all = torch.empty(t["x"].shape, dtype=torch.bfloat16 if wl.y_bf16 else torch.float32, device="cuda")
+    yh = torch.empty(y_all.shape, dtype=y_all.dtype, pin_memory=True)
     torch.cuda.synchronize()
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
-    d2h = y_all.numel() * 4
+    d2h = y_all.numel() * y_all.element_size()
 
     def one():
         for k in keys:

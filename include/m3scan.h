@@ -77,6 +77,28 @@ typedef enum m3_algo {
   M3_ALGO_CHUNKED = 2    /* chunked tcgen05/TMEM path (bf16 inputs, supported shapes only)   */
 } m3_algo;
 
+/*
+ * Fused prologue: the step of a Mamba-3 mixer just before the scan, done by
+ * the scan kernels while they load their inputs.  The B/C normalisation is
+ * the pages' BC/QK norm ("Mamba-3: an inference-first LLM", section
+ * "Implementation and kernel optimisation"; "Together AI announces Mamba-3",
+ * Mamba-2 vs Mamba-3 table, normalisation row: QKNorm replaces RMSNorm).
+ * The pages do not say how dt is produced; softplus of a biased projection
+ * keeps it positive and is the plainest choice.  Flags of the `prologue`
+ * argument field; 0 = the inputs are used as given.
+ *   M3_PRO_DT_SOFTPLUS: dt holds the pre-activation; the scan uses
+ *       softplus(dt + dt_bias[h]) = log(1 + exp(dt + dt_bias[h])).
+ *   M3_PRO_BC_NORM: every row of B and of C (one token, group and rank: N
+ *       values) is divided by its root mean square, v / sqrt(mean(v^2) +
+ *       1e-6), before use; so is the carried previous-token B.  There is no
+ *       gain vector (a per-column gain folds into the B and C projection).
+ * The carry in m3_state keeps the raw B and x of the last token.
+ */
+typedef enum m3_prologue {
+  M3_PRO_DT_SOFTPLUS = 1,
+  M3_PRO_BC_NORM = 2
+} m3_prologue;
+
 /* Problem sizes. */
 typedef struct m3_dims {
   int32_t batch;    /* sequences (state slots)                                   */
@@ -114,12 +136,17 @@ typedef struct m3_prefill_args {
   const float* D;    /* [H] f32 */
   const int32_t* cu_seqlens; /* device [nseq+1], nondecreasing, cu[0] = 0, cu[nseq] = L; or NULL */
   int32_t nseq;              /* sequences in the packed batch (ignored without cu_seqlens) */
-  float* y;                  /* [batch][L][H][R][P] f32 output */
+  void* y;                   /* [batch][L][H][R][P] output, f32 or bf16 (y_dtype) */
   int32_t ngroups; /* G: B and C shared by groups of H/G consecutive heads, laid out
                       [batch][L][G][R][N] (head h uses group h / (H / G)); must divide H;
                       0 (or H) = one B and C per head, [batch][L][H][R][N].  The pages
                       give B and C per head; groups are an addressing variant only (the
                       recurrence of each head is unchanged) */
+  int32_t y_dtype; /* m3_dtype of y: M3_F32 (0, the default) or M3_BF16, the f32 result
+                      rounded to nearest even (half the output bytes).  Not on the pages,
+                      which fix no output type */
+  int32_t prologue;      /* m3_prologue flags; 0 = none */
+  const float* dt_bias;  /* [H] f32 added to dt before softplus (M3_PRO_DT_SOFTPLUS); NULL = 0 */
 } m3_prefill_args;
 
 /* One decode step: a single new token per sequence. */
@@ -133,8 +160,11 @@ typedef struct m3_decode_args {
   const void* theta; /* [batch][H][N/2]  in_dtype; NULL: theta = 0 */
   const float* A;    /* [H] f32 */
   const float* D;    /* [H] f32 */
-  float* y;          /* [batch][H][R][P] f32 output */
+  void* y;           /* [batch][H][R][P] output, f32 or bf16 (y_dtype) */
   int32_t ngroups;   /* as in m3_prefill_args: B and C [batch][G][R][N]; 0 = per head */
+  int32_t y_dtype;   /* as in m3_prefill_args: M3_F32 (0) or M3_BF16 */
+  int32_t prologue;      /* as in m3_prefill_args */
+  const float* dt_bias;  /* [H] f32 or NULL */
 } m3_decode_args;
 
 /*

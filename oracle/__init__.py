@@ -199,6 +199,44 @@ def decode(inp: dict, *, batch, H, P, N, R, dtype, steps, units=None, nthreads=N
     return y, h.reshape(len(sel), K, P, 2), pB, px
 
 
+BC_NORM_EPS = 1e-6
+
+
+def softplus(z):
+    """log(1 + e^z) in double, written as max(z, 0) + log1p(e^-|z|): no
+    overflow for large z, no cancellation for very negative z."""
+    z = np.asarray(z, np.float64)
+    return np.maximum(z, 0.0) + np.log1p(np.exp(-np.abs(z)))
+
+
+def rms_normalize(a, eps=BC_NORM_EPS):
+    """Each row (last axis) divided by its root mean square,
+    a / sqrt(mean(a^2) + eps): the BC/QK norm ("Mamba-3: an inference-first
+    LLM", section "Implementation and kernel optimisation")."""
+    a = np.asarray(a, np.float64)
+    return a / np.sqrt(np.mean(a * a, axis=-1, keepdims=True) + eps)
+
+
+def apply_prologue(inp: dict, dtype: str, *, dt_softplus=False, bc_norm=False, dt_bias=None) -> dict:
+    """The inputs as the scan sees them after the fused prologue, in double
+    (run the oracle on the result with dtype "f64").  dt becomes
+    softplus(dt + dt_bias[h]) (heads on dt's last axis, in prefill and
+    decode layouts); every row over N of B, C and the carried prev_B is
+    RMS-normalised.  The other inputs are widened unchanged; lam and theta
+    given as None stay None, h0, A and D are kept as they are."""
+    out = {}
+    for k, v in inp.items():
+        out[k] = v if (v is None or k in ("A", "D", "h0", "dt_bias")) else _widen(v, dtype)
+    if dt_softplus:
+        bias = 0.0 if dt_bias is None else np.asarray(dt_bias, np.float64)
+        out["dt"] = softplus(out["dt"] + bias)
+    if bc_norm:
+        for k in ("B", "C", "prev_B"):
+            if out.get(k) is not None:
+                out[k] = rms_normalize(out[k])
+    return out
+
+
 def _lam_theta(inp, K):
     """lam and theta of ``inp``; None stands for lam = 1 and theta = 0 (the
     first-order, real-state special case), written out as arrays."""

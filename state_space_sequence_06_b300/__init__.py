@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libm3scan.so")
 M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_ERR_ALLOC, M3_ERR_SCRATCH = range(7)
 M3_F32, M3_BF16 = 0, 1
 M3_ALGO_AUTO, M3_ALGO_RECURRENT, M3_ALGO_CHUNKED = 0, 1, 2
+M3_PRO_DT_SOFTPLUS, M3_PRO_BC_NORM = 1, 2
 
 SYMBOLS = ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
            "m3_decode_step", "m3_device_status", "m3_status_string")
@@ -44,13 +45,15 @@ class m3_prefill_args(ctypes.Structure):
     _fields_ = [("dims", m3_dims), ("seqlen", ctypes.c_int64), ("chunk", ctypes.c_int32),
                 ("algo", ctypes.c_int32)] + \
         [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "cu_seqlens")] + \
-        [("nseq", ctypes.c_int32), ("y", ctypes.c_void_p), ("ngroups", ctypes.c_int32)]
+        [("nseq", ctypes.c_int32), ("y", ctypes.c_void_p), ("ngroups", ctypes.c_int32),
+         ("y_dtype", ctypes.c_int32), ("prologue", ctypes.c_int32), ("dt_bias", ctypes.c_void_p)]
 
 
 class m3_decode_args(ctypes.Structure):
     _fields_ = [("dims", m3_dims)] + \
         [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "y")] + \
-        [("ngroups", ctypes.c_int32)]
+        [("ngroups", ctypes.c_int32), ("y_dtype", ctypes.c_int32), ("prologue", ctypes.c_int32),
+         ("dt_bias", ctypes.c_void_p)]
 
 
 _lib = None
@@ -174,17 +177,22 @@ def m3_state_view(state: State) -> m3_state_ptrs:
 
 
 def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
-                    cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None, _entry="m3_scan_prefill"):
+                    cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, prologue: int = 0,
+                    dt_bias=None, stream=None, _entry="m3_scan_prefill"):
     """Prefill.  x [b][L][H][R][P], B/C [b][L][G][R][N] (G groups of heads;
-    G = H: one per head), dt/lam [b][L][H], theta [b][L][H][N/2] (all bf16 or all f32; lam None: lam = 1, theta
-    None: theta = 0), A/D [H] f32, y [b][L][H][R][P]
-    f32 (written).  ``cu_seqlens`` (int32 CUDA tensor) packs sequences in a
-    batch of one row."""
+    G = H: one per head), dt/lam [b][L][H], theta [b][L][H][N/2] (all bf16
+    or all f32; lam None: lam = 1, theta None: theta = 0), A/D [H] f32,
+    y [b][L][H][R][P] f32 or bf16 (written; bf16 is the f32 result rounded
+    to nearest even).  ``cu_seqlens`` (int32 CUDA tensor) packs sequences
+    in a batch of one row.  ``prologue`` (M3_PRO_* flags) makes the kernel
+    apply softplus(dt + dt_bias) and/or the RMS norm of B and C rows."""
     b, L, H, R, P = x.shape
     N = B.shape[-1]
     a = m3_prefill_args()
     a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
     a.ngroups = B.shape[2]  # B and C [b][L][G][R][N]: G = H is one per head
+    a.y_dtype = _dtype_code(y)
+    a.prologue, a.dt_bias = prologue, _ptr(dt_bias)
     a.seqlen, a.chunk, a.algo = L, chunk, algo
     a.x, a.B, a.C, a.dt, a.lam, a.theta = (_ptr(t) for t in (x, B, C, dt, lam, theta))
     a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
@@ -196,23 +204,28 @@ def m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = N
 
 
 def m3_scan_prefill_noalloc(x, B, C, dt, lam, theta, A, D, y, *, state: State | None = None,
-                            cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, stream=None):
+                            cu_seqlens=None, chunk: int = 0, algo: int = M3_ALGO_AUTO, prologue: int = 0,
+                            dt_bias=None, stream=None):
     """m3_scan_prefill without device-memory allocation in the call: its
     scratch is a fixed buffer in the library (calls that overlap in time
     race on it; M3_ERR_SCRATCH when a request needs more)."""
     m3_scan_prefill(x, B, C, dt, lam, theta, A, D, y, state=state, cu_seqlens=cu_seqlens, chunk=chunk,
-                    algo=algo, stream=stream, _entry="m3_scan_prefill_noalloc")
+                    algo=algo, prologue=prologue, dt_bias=dt_bias, stream=stream,
+                    _entry="m3_scan_prefill_noalloc")
 
 
-def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None):
+def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None, prologue: int = 0,
+                   dt_bias=None):
     """One decode step.  x [b][H][R][P], B/C [b][G][R][N] (G groups of heads;
-    G = H: one per head), dt/lam [b][H], theta [b][H][N/2] (lam / theta None: 1 / 0), A/D [H] f32, y [b][H][R][P]
-    f32 (written)."""
+    G = H: one per head), dt/lam [b][H], theta [b][H][N/2] (lam / theta
+    None: 1 / 0), A/D [H] f32, y [b][H][R][P] f32 or bf16 (written)."""
     b, H, R, P = x.shape
     N = B.shape[-1]
     a = m3_decode_args()
     a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
     a.ngroups = B.shape[1]
+    a.y_dtype = _dtype_code(y)
+    a.prologue, a.dt_bias = prologue, _ptr(dt_bias)
     a.x, a.B, a.C, a.dt, a.lam, a.theta = (_ptr(t) for t in (x, B, C, dt, lam, theta))
     a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
     _check(load_library().m3_decode_step(ctypes.byref(a), state.handle, _stream(stream)),

@@ -57,13 +57,16 @@ struct ChunkParams {
   const float* A;
   const float* D;
   const int32_t* cu_seqlens;  // NULL: fixed length L per batch row
-  float* y;
+  void* y;                  // f32, or bf16 when ybf
+  int ybf;
   float* h;                 // state slots or NULL
   __nv_bfloat16* prev_B;    // carry slots or NULL
   __nv_bfloat16* prev_x;
   int64_t L;
   int H;
   int G;  // B and C groups (head h uses group h / (H / G))
+  int pro;               // m3_prologue flags
+  const float* dt_bias;  // [H] or NULL
   // Balanced schedule (bal_grid == 0: one CTA per (sequence, head) unit).
   // With fixed-length sequences the bal_units units' chunks, unit after
   // unit, are cut into bal_grid equal ranges, one per CTA (all resident at
@@ -247,6 +250,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   __shared__ float sDt[Q + 1], sBet[Q + 1], sWarpTot[4];
   __shared__ float sPsum[G][K2];
   __shared__ float sPhi[K2];  // cumulative angle per pair at the end of the last chunk, in [-pi, pi)
+  __shared__ float sBScl[MR], sCScl[MR];  // BC norm: 1 / rms of each (token, rank) row of the tile
+  __shared__ float sCarryScl[8];          // BC norm of the carried B rows at a segment start
   __shared__ float sPhiEndX[XB][K2];  // the same after chunk c (slot c % XB), for the state warps
 
   // this CTA's segments: {unit, first token, end token, flags}, the first
@@ -376,8 +381,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     const unsigned short* lam_bits = reinterpret_cast<const unsigned short*>(p.lam);
     // (token Q of the last chunk of a segment lies past its end: zero, the
     // carry takes the next token's previous-token term)
+    // (with dt through softplus an absent token is marked kNoToken: its dt
+    // must stay 0, not become softplus(bias))
+    constexpr uint32_t kNoToken = 0xFFFFFFFFu;
+    const bool dt_sp = (p.pro & M3_PRO_DT_SOFTPLUS) != 0;
     auto load_scalars = [&](int c, uint32_t& d, uint32_t& l) {
-      d = 0u;
+      d = dt_sp ? kNoToken : 0u;
       l = 0u;
       if (pt <= Q && c < nchunks) {
         const int si = seg_of(c);
@@ -393,7 +402,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     load_scalars(0, d_cur, l_cur);
     // prologue of chunk c: scalars, angle scan, rotation of B and C, X and W X.
     // Returns false when the pipeline was aborted.
-    auto prologue = [&](int c) -> bool {
+    auto prologue = [&](int c, auto normtag) -> bool {
+      constexpr bool NORM = decltype(normtag)::value;
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
       const int si = seg_of(c);
@@ -407,8 +417,35 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       // scalar slot xs last served chunk c - XB: its output must be done
       if (got && c >= XB) got = wait_xfree(c - XB);
       if (!group_and(1, NPRO, got)) return false;
+      if constexpr (NORM) {
+        // ---- BC norm: 1 / rms of every B and C row (token, rank) of the tile
+        //      as it landed; TPR adjacent threads per row, 16-byte chunks
+        constexpr int TPR = NPRO / (2 * MR), CPT = N / 8 / TPR;
+        const int row = pt / TPR, part = pt % TPR;
+        const bool isC = row >= MR;
+        const int rr = isC ? row - MR : row;
+        const uint8_t* base = stg + (isC ? Cfg::OFF_C : Cfg::OFF_B);
+        const uint32_t blk_bytes = isC ? (uint32_t)(MR * 128) : (uint32_t)Cfg::BB;
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPT; ++q) {
+          const int col = (part * CPT + q) * 8;
+          const uint4 v = *reinterpret_cast<const uint4*>(base + (col / 64) * blk_bytes + sw128_offset(rr, col % 64));
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = bf2_to_f2(w4[e]);
+            ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+          }
+        }
+#pragma unroll
+        for (int o = TPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (part == 0) (isC ? sCScl : sBScl)[rr] = rsqrtf(ss * (1.f / N) + kBcNormEps);
+      }
       // ---- per-token scalars and the inclusive scan of dt * A
-      const float dcur = __uint_as_float(d_cur << 16), lcur = __uint_as_float(l_cur << 16);
+      float dcur = __uint_as_float(d_cur << 16);
+      const float lcur = __uint_as_float(l_cur << 16);
+      if (dt_sp) dcur = d_cur == kNoToken ? 0.f : softplus_f(dcur + (p.dt_bias ? __ldg(p.dt_bias + seg_head(si)) : 0.f));
       if (pt <= Q) {
         sDt[pt] = dcur;
         sBet[pt] = (1.f - lcur) * dcur;
@@ -512,8 +549,15 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           for (int r = 0; r < R; ++r) {
             const uint32_t rc = sw128_offset(i * R + r, col);
             const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
-            const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
-            const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
+            float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
+            float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
+            if constexpr (NORM) {
+              const float fb = sBScl[i * R + r], fc = sCScl[i * R + r];
+              b.x *= fb;
+              b.y *= fb;
+              cc.x *= fc;
+              cc.y *= fc;
+            }
             uint32_t hi, lo;
             split_half2(cs[ii] * b.x - sn[ii] * b.y, sn[ii] * b.x + cs[ii] * b.y, hi, lo);
             *reinterpret_cast<uint32_t*>(Bt + ob) = hi;
@@ -612,11 +656,19 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       return true;
     };
     // the prologue runs one chunk ahead of S -> S', which waits for MMA 1
-    bool alive = prologue(0);
-    for (int c = 0; c < nchunks && alive; ++c) {
-      if (c + 1 < nchunks && !prologue(c + 1)) break;
-      alive = scores(c);
-    }
+    // compiled once with and once without the BC norm (the real-state
+    // variant has none: its B and C reach the MMAs without a lo part)
+    auto run = [&](auto normtag) {
+      bool alive = prologue(0, normtag);
+      for (int c = 0; c < nchunks && alive; ++c) {
+        if (c + 1 < nchunks && !prologue(c + 1, normtag)) break;
+        alive = scores(c);
+      }
+    };
+    if (!RE && (p.pro & M3_PRO_BC_NORM))
+      run(BoolTag<true>{});
+    else
+      run(BoolTag<false>{});
   } else if (warp < Cfg::W_MMA) {
     // ======================= state warps: state step and output epilogue
     const int tt = tid - NPRO;
@@ -657,9 +709,17 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const __nv_bfloat16* cB = from_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
       const __nv_bfloat16* cx = from_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
       const int64_t row0 = sSegTok0[si] * H + head;
-      const float dt0 = __bfloat162float(p.dt[row0]);
+      const float dt0 = scan_dt(__bfloat162float(p.dt[row0]), p.pro, p.dt_bias, head);
       const float lm0 = p.lam ? __bfloat162float(p.lam[row0]) : 1.f;
       const float bet0 = (1.f - lm0) * dt0;
+      const bool norm_c = (p.pro & M3_PRO_BC_NORM) && cB;  // BC norm of the carried B rows
+      if (norm_c) {
+        for (int r = tt >> 5; r < R; r += NSTA / 32) {
+          const float sc = warp_rms_scale(cB + r * N, N, tt & 31);
+          if ((tt & 31) == 0) sCarryScl[r] = sc;
+        }
+        group_sync(2, NSTA);
+      }
       for (int cb = 0; cb < P; cb += 16) {
         float v[16];
 #pragma unroll
@@ -670,7 +730,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2];
           if (cB) {
             for (int r = 0; r < R; ++r) {
-              const float b = bet0 * __bfloat162float(cB[r * N + g_row]);
+              const float b = bet0 * (norm_c ? sCarryScl[r] : 1.f) * __bfloat162float(cB[r * N + g_row]);
               const __nv_bfloat16* xp = cx + r * P + cb;
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = fmaf(b, __bfloat162float(xp[i]), v[i]);
@@ -818,7 +878,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     };
 
     // output of chunk c: y = Y + e^{Lam_t} Yi + D x, needs MMAs 2 and 3 of chunk c
-    auto output = [&](int c) -> bool {
+    auto output = [&](int c, auto ybf) -> bool {
       const int s = c & 1, xs = c % XB;
       const int si = seg_of(c), head = seg_head(si);
       const int64_t cc = c - sSegC0[si];
@@ -836,13 +896,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const int r0 = 16 * q4 + lane / 4, cl = 2 * (lane % 4);
       bool valid[2];
       float el[2];
-      float* yrow[2];
+      int64_t yrow[2];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int t = r0 + 8 * rr, it = t / R, rk = t % R;
         valid[rr] = it < nvalid;
         el[rr] = sELam[xs][it];
-        yrow[rr] = p.y + ((ct0 + it) * H + head) * (R * P) + rk * P;
+        yrow[rr] = ((ct0 + it) * H + head) * (R * P) + rk * P;
       }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -869,7 +929,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             const int i0 = 4 * g8 + 2 * rr;
             const float o0 = fmaf(Dh, f.x, fmaf(el[rr], b[i0], a[i0]));
             const float o1 = fmaf(Dh, f.y, fmaf(el[rr], b[i0 + 1], a[i0 + 1]));
-            if (valid[rr]) *reinterpret_cast<float2*>(yrow[rr] + col) = make_float2(o0, o1);
+            if (valid[rr]) st_y2(p.y, yrow[rr] + col, o0, o1, decltype(ybf)::value);
           }
         }
       }
@@ -886,20 +946,28 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // the per-chunk loop, whose code stays small and contiguous (the roles
     // of one SM share its instruction cache).  `alive` is the same in every
     // state warp: each step ends in a group vote.
-    bool alive = true;
-    int n = 0;
-    for (int si = 0; si < nseg && alive; ++si) {
-      if (!init_seg(si)) break;
-      const int end = sSegC0[si + 1];
-      for (; n < end; ++n) {
-        if (!xconv(n) || (n >= 1 && !output(n - 1)) || !state(n)) {
-          alive = false;
-          break;
+    // The loop is compiled once per output type (y f32 or bf16), so that the
+    // store needs no branch in the chunk loop.
+    auto run = [&](auto ybf) {
+      bool alive = true;
+      int n = 0;
+      for (int si = 0; si < nseg && alive; ++si) {
+        if (!init_seg(si)) break;
+        const int end = sSegC0[si + 1];
+        for (; n < end; ++n) {
+          if (!xconv(n) || (n >= 1 && !output(n - 1, ybf)) || !state(n)) {
+            alive = false;
+            break;
+          }
         }
+        if (alive) finalize(si, n - 1);
       }
-      if (alive) finalize(si, n - 1);
-    }
-    if (alive) output(nchunks - 1);
+      if (alive) output(nchunks - 1, ybf);
+    };
+    if (p.ybf)
+      run(BoolTag<true>{});
+    else
+      run(BoolTag<false>{});
   } else if (warp == Cfg::W_MMA || warp == Cfg::W_MMA2) {
     // ======================= MMA warps (one thread each issues)
     // K-major operand tiles: 16-element K step = 32 B inside a 128 B row, 64-column blocks MR*128 B apart
@@ -1168,12 +1236,15 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   p.D = a->D;
   p.cu_seqlens = a->cu_seqlens;
   p.y = a->y;
+  p.ybf = a->y_dtype == M3_BF16;
   p.h = h;
   p.prev_B = static_cast<__nv_bfloat16*>(prev_B);
   p.prev_x = static_cast<__nv_bfloat16*>(prev_x);
   p.L = a->seqlen;
   p.H = H;
   p.G = G;
+  p.pro = a->prologue;
+  p.dt_bias = a->dt_bias;
   auto kern = chunked_prefill_kernel<N, R, Q, RE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;
@@ -1228,7 +1299,8 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
 
 // Shapes with a chunked kernel: bf16 inputs, P = 64, and (N, R, chunk) in
 // {(128, 1, 64), (64, 1, 64), (64, 4, 16), (64, 2, 32), (128, 2, 32)}; with
-// theta = 0 (NULL) in {(128, 1, 64), (64, 1, 64), (64, 4, 16)}.
+// theta = 0 (NULL) in {(128, 1, 64), (64, 1, 64), (64, 4, 16)}, without the
+// BC norm.
 inline m3_status chunked_prefill(const m3_prefill_args* a, float* h, void* prev_B, void* prev_x, int nseq,
                                  cudaStream_t s, void* fixed = nullptr, size_t fixed_bytes = 0) {
   const m3_dims& d = a->dims;
@@ -1236,6 +1308,9 @@ inline m3_status chunked_prefill(const m3_prefill_args* a, float* h, void* prev_
   const int R = d.rank, N = d.dstate;
   const int Q = a->chunk > 0 ? a->chunk : (R == 1 ? 64 : 64 / R);
   const bool re = a->theta == nullptr;
+  // the real-state variant feeds B and C to the MMAs as single f16 values,
+  // exact only for the bf16 inputs themselves, not for normalised rows
+  if (re && (a->prologue & M3_PRO_BC_NORM)) return M3_ERR_UNSUPPORTED;
 #define M3_CH(NN, RR, QQ) \
   if (!re && N == NN && R == RR && Q == QQ)                                                  \
     return chunked_launch<NN, RR, QQ, false>(a, h, prev_B, prev_x, nseq, s, fixed, fixed_bytes);

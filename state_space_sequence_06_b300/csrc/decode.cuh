@@ -32,7 +32,8 @@ struct DecodeParams {
   const void* theta;
   const float* A;
   const float* D;
-  float* y;
+  void* y;   // f32, or bf16 when ybf
+  int ybf;
   float* h;
   void* prev_B;
   void* prev_x;
@@ -42,6 +43,8 @@ struct DecodeParams {
   int PP;  // P / 2
   int KG;  // k groups (blockDim.x / PP)
   int bulk;  // 1: every per-unit input row is a multiple of 16 bytes, so they arrive by bulk copy too
+  int pro;   // m3_prologue flags
+  const float* dt_bias;
 };
 
 // R is the rank when known at compile time; R == 0 reads it from p.R (<= 8).
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
       if (th_bytes) bulk_g2s(saddr(rawTh), thg, th_bytes, saddr(&bar));
     }
   }
-  const float dt = ldf(static_cast<const T*>(p.dt), unit);
+  const float dt = scan_dt(ldf(static_cast<const T*>(p.dt), unit), p.pro, p.dt_bias, head);
   const float lam = p.lam ? ldf(static_cast<const T*>(p.lam), unit) : 1.f;  // no lam: lam = 1
   const float A = p.A[head], D = p.D[head];
   const float decay = expf(dt * A);
@@ -128,13 +131,25 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
   const T* sX = p.bulk ? rawX : xg;
   const T* sPX = p.bulk ? rawPX : pxg;
   const T* sTh = p.bulk ? rawTh : thg;
+  // BC norm: one scale per row (B_r, C_r, carried B_r), a warp per row
+  __shared__ float s_scale[3 * RMAX];
+  const bool norm = (p.pro & M3_PRO_BC_NORM) != 0;
+  if (norm) {
+    for (int row = tid / 32; row < 3 * R; row += blockDim.x / 32) {
+      const T* src = row < R ? sB + row * N : (row < 2 * R ? sC + (row - R) * N : sPB + (row - 2 * R) * N);
+      const float sc = warp_rms_scale(src, N, tid % 32);
+      if (tid % 32 == 0) s_scale[row] = sc;
+    }
+    __syncthreads();
+  }
   float2* kd2 = reinterpret_cast<float2*>(kd);
   for (int i = tid; i < K * R; i += blockDim.x) {
     const int k = i / R, r = i % R;
+    const float fb = norm ? s_scale[r] : 1.f, fc = norm ? s_scale[R + r] : 1.f, fp = norm ? s_scale[2 * R + r] : 1.f;
     float2* rec = kd2 + (size_t)k * 2 * KW;
-    rec[1 + r] = make_float2(to_f(sPB[r * N + 2 * k]), to_f(sPB[r * N + 2 * k + 1]));
-    rec[1 + R + r] = make_float2(to_f(sB[r * N + 2 * k]), to_f(sB[r * N + 2 * k + 1]));
-    rec[1 + 2 * R + r] = make_float2(to_f(sC[r * N + 2 * k]), to_f(sC[r * N + 2 * k + 1]));
+    rec[1 + r] = make_float2(fp * to_f(sPB[r * N + 2 * k]), fp * to_f(sPB[r * N + 2 * k + 1]));
+    rec[1 + R + r] = make_float2(fb * to_f(sB[r * N + 2 * k]), fb * to_f(sB[r * N + 2 * k + 1]));
+    rec[1 + 2 * R + r] = make_float2(fc * to_f(sC[r * N + 2 * k]), fc * to_f(sC[r * N + 2 * k + 1]));
   }
   for (int i = tid; i < R * P; i += blockDim.x) {
     xs[i] = to_f(sX[i]);
@@ -228,11 +243,11 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
     bulk_s2g(hg, saddr(hsm), state_bytes);
     bulk_commit();
   }
-  float* yg = p.y + (int64_t)unit * R * P;
+  const int64_t y0 = (int64_t)unit * R * P;
   for (int i = tid; i < R * P; i += blockDim.x) {
     float sum = 0.f;
     for (int g = 0; g < KG; ++g) sum += red[g * R * P + i];
-    yg[i] = fmaf(D, xs[i], sum);
+    st_y(p.y, y0 + i, fmaf(D, xs[i], sum), p.ybf);
   }
   if (tid == 0) bulk_wait_read_all();  // shared memory must outlive the copy's reads
 }

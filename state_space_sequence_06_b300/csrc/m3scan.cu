@@ -231,12 +231,15 @@ m3_status m3_decode_step(const m3_decode_args* a, m3_state* st, void* stream) {
   // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
   if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
   if (a->ngroups < 0 || (a->ngroups > 0 && a->dims.nheads % a->ngroups != 0)) return M3_ERR_INVALID_ARG;
+  if (a->y_dtype != M3_F32 && a->y_dtype != M3_BF16) return M3_ERR_INVALID_ARG;
+  if (a->prologue & ~(M3_PRO_DT_SOFTPLUS | M3_PRO_BC_NORM)) return M3_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
       !aligned16(a->y))
     return M3_ERR_INVALID_ARG;
   m3::DecodeParams p{};
   p.x = a->x; p.B = a->B; p.C = a->C; p.dt = a->dt; p.lam = a->lam; p.theta = a->theta;
-  p.A = a->A; p.D = a->D; p.y = a->y;
+  p.A = a->A; p.D = a->D; p.y = a->y; p.ybf = a->y_dtype == M3_BF16;
+  p.pro = a->prologue; p.dt_bias = a->dt_bias;
   p.h = st->h; p.prev_B = st->prev_B; p.prev_x = st->prev_x;
   p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
   p.G = a->ngroups > 0 ? a->ngroups : a->dims.nheads;
@@ -257,6 +260,8 @@ m3_status prefill_impl(const m3_prefill_args* a, m3_state* st, void* stream, voi
   // lam and theta may be NULL (lam = 1, theta = 0: the Mamba-2 special case)
   if (!a->x || !a->B || !a->C || !a->dt || !a->A || !a->D || !a->y) return M3_ERR_INVALID_ARG;
   if (a->ngroups < 0 || (a->ngroups > 0 && a->dims.nheads % a->ngroups != 0)) return M3_ERR_INVALID_ARG;
+  if (a->y_dtype != M3_F32 && a->y_dtype != M3_BF16) return M3_ERR_INVALID_ARG;
+  if (a->prologue & ~(M3_PRO_DT_SOFTPLUS | M3_PRO_BC_NORM)) return M3_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->theta) ||
       !aligned16(a->y))
     return M3_ERR_INVALID_ARG;
@@ -281,7 +286,8 @@ m3_status prefill_impl(const m3_prefill_args* a, m3_state* st, void* stream, voi
   }
   m3::RecurrentParams p{};
   p.x = a->x; p.B = a->B; p.C = a->C; p.dt = a->dt; p.lam = a->lam; p.theta = a->theta;
-  p.A = a->A; p.D = a->D; p.cu_seqlens = a->cu_seqlens; p.y = a->y;
+  p.A = a->A; p.D = a->D; p.cu_seqlens = a->cu_seqlens; p.y = a->y; p.ybf = a->y_dtype == M3_BF16;
+  p.pro = a->prologue; p.dt_bias = a->dt_bias;
   p.h = st ? st->h : nullptr;
   p.prev_B = st ? st->prev_B : nullptr;
   p.prev_x = st ? st->prev_x : nullptr;

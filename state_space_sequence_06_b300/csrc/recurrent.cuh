@@ -29,7 +29,8 @@ struct RecurrentParams {
   const float* A;
   const float* D;
   const int32_t* cu_seqlens;  // NULL: fixed length L per batch row
-  float* y;
+  void* y;        // f32, or bf16 when ybf
+  int ybf;
   float* h;       // state slots or NULL
   void* prev_B;   // carry slots or NULL
   void* prev_x;
@@ -38,7 +39,20 @@ struct RecurrentParams {
   int G;          // B and C groups (head h uses group h / (H / G))
   int KS;         // threads per p (power of two <= 32)
   int TB;         // tokens staged per block
+  int pro;        // m3_prologue flags
+  const float* dt_bias;
 };
+
+// BC norm in shared memory: rows [0, nrows) of n values each, scaled in place
+// by 1 / sqrt(mean(v^2) + eps), a warp per row.  Callers synchronise around it.
+__device__ __forceinline__ void normalize_rows_smem(float* base, int nrows, int n) {
+  const int lane = threadIdx.x % 32;
+  for (int row = threadIdx.x / 32; row < nrows; row += blockDim.x / 32) {
+    float* v = base + (size_t)row * n;
+    const float sc = warp_rms_scale(v, n, lane);
+    for (int i = lane; i < n; i += 32) v[i] *= sc;
+  }
+}
 
 // R is the rank when known at compile time; R == 0 reads it from p.R (<= 8).
 template <typename T, int KPT, int R_>
@@ -86,6 +100,11 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
     Bs[i] = p.prev_B ? ldf(static_cast<const T*>(p.prev_B), (int64_t)unit * RN + i) : 0.f;
   for (int i = tid; i < RP; i += blockDim.x)
     xs[i] = p.prev_x ? ldf(static_cast<const T*>(p.prev_x), (int64_t)unit * RP + i) : 0.f;
+  const bool norm = (p.pro & M3_PRO_BC_NORM) != 0;
+  if (norm) {  // the carried B, as every staged B row below
+    __syncthreads();
+    normalize_rows_smem(Bs, R, N);
+  }
 
   const T* xg = static_cast<const T*>(p.x);
   const T* Bg = static_cast<const T*>(p.B);
@@ -110,7 +129,7 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
     for (int i = tid; i < nb * K; i += blockDim.x) {
       const int tb = i / K, k = i % K;
       const int64_t ts = (tok0 + t0 + tb) * H + head;
-      const float dt = ldf(dtg, ts);
+      const float dt = scan_dt(ldf(dtg, ts), p.pro, p.dt_bias, head);
       float s = 0.f, c = 1.f;  // theta = 0 when theta is not given
       if (thg) sincosf(dt * ldf(thg, ts * K + k), &s, &c);
       const float dec = expf(dt * A);
@@ -122,6 +141,11 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
       }
     }
     __syncthreads();
+    if (norm) {  // rows 1..nb of Bs (row 0 is the previous token, already normalised) and rows 0..nb-1 of Cs
+      normalize_rows_smem(Bs + RN, nb * R, N);
+      normalize_rows_smem(Cs, nb * R, N);
+      __syncthreads();
+    }
 
     for (int tb = 0; tb < nb; ++tb) {
       const float gam = sc[2 * tb], bet = sc[2 * tb + 1];
@@ -163,10 +187,10 @@ __global__ void recurrent_prefill_kernel(const RecurrentParams p) {
       for (int r = 0; r < RMAX; ++r)
         for (int o = KS / 2; o > 0; o >>= 1) yacc[r] += __shfl_xor_sync(0xffffffffu, yacc[r], o, KS);
       if (active && ks == 0) {
-        float* yo = p.y + ((tok0 + t0 + tb) * H + head) * RP;
+        const int64_t yo = ((tok0 + t0 + tb) * H + head) * RP;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
-          if (r < R) yo[r * P + pi] = fmaf(D, xcv[r], yacc[r]);
+          if (r < R) st_y(p.y, yo + r * P + pi, fmaf(D, xcv[r], yacc[r]), p.ybf);
       }
     }
     __syncthreads();

@@ -24,7 +24,7 @@ _SRC = os.path.join(_HERE, "m3_synth.c")
 _LIB_PATH = os.path.join(_HERE, "libm3synth.so")
 
 # tensor stream ids (part of the generator's definition: changing one changes the data)
-S_X, S_B, S_C, S_DT, S_A, S_THETA, S_LAM, S_D, S_H0, S_PREVB, S_PREVX, S_LENS = range(1, 13)
+S_X, S_B, S_C, S_DT, S_A, S_THETA, S_LAM, S_D, S_H0, S_PREVB, S_PREVX, S_LENS, S_DTBIAS = range(1, 14)
 
 # distribution kinds, as in m3_synth.c
 K_NORMAL, K_NORMAL_RMS, K_SOFTPLUS, K_NEG_EXP, K_UNIFORM, K_SIGMOID = range(6)
@@ -120,6 +120,11 @@ class Workload:
     real: bool = False   # theta = 0: a real state (given as None)
     euler: bool = False  # lam = 1: first-order exponential Euler (given as None)
     ngroups: int = 0  # B/C groups shared by nheads/ngroups consecutive heads; 0: one per head
+    y_bf16: bool = False  # output y in bf16 (else f32)
+    # raw inputs for the fused prologue: dt the pre-activation N(dt_shift, 1)
+    # with a per-head bias N(0, 0.5), B and C (and the carried B) N(0, 2^2)
+    # without row normalisation
+    prologue: bool = False
     cu_seqlens: np.ndarray | None = field(default=None, repr=False)
     # shard of a global problem: this shard's `batch` sequences (varlen:
     # `nseq` sequences) are number shard_index*batch.. of a global batch of
@@ -169,6 +174,12 @@ def workloads() -> dict:
         "decode_siso_g1_b256": Workload(
             "decode_siso_g1_b256", "decode", 256, 1024, 32, 64, 128, 1, "bf16", h0_std=0.1, carry=True,
             ngroups=1),
+        # the same SISO prefill with y written in bf16
+        "siso_ybf16_b8_l4096": Workload("siso_ybf16_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16",
+                                        chunk=64, y_bf16=True),
+        # the same SISO prefill from raw inputs: dt before softplus, B and C before the RMS norm
+        "siso_prologue_b8_l4096": Workload("siso_prologue_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16",
+                                           chunk=64, prologue=True),
         "varlen_16": Workload(
             "varlen_16", "varlen", 1, 0, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0,
             nseq=16, len_lo=256, len_hi=8192,
@@ -238,9 +249,12 @@ def prefill_inputs(wl: Workload) -> dict:
 
     d = {
         "x": tok((b, L, H, R, P), S_X, K_NORMAL, 0.0, 1.0),
-        "B": tok((b, L, G, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
-        "C": tok((b, L, G, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
-        "dt": tok((b, L, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
+        "B": tok((b, L, G, R, N), S_B, K_NORMAL, 0.0, 2.0) if wl.prologue else
+        tok((b, L, G, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "C": tok((b, L, G, R, N), S_C, K_NORMAL, 0.0, 2.0) if wl.prologue else
+        tok((b, L, G, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "dt": tok((b, L, H), S_DT, K_NORMAL, wl.dt_shift, 1.0) if wl.prologue else
+        tok((b, L, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
         "lam": tok((b, L, H), S_LAM, K_SIGMOID, 0.0, 0.0),
         "theta": tok((b, L, H, N // 2), S_THETA, K_UNIFORM, 0.0, np.pi),
         "A": fill((H,), S_A, K_NEG_EXP, 0.0, 0.5, "f32", s),
@@ -250,11 +264,14 @@ def prefill_inputs(wl: Workload) -> dict:
         d["theta"] = None
     if wl.euler:
         d["lam"] = None
+    if wl.prologue:
+        d["dt_bias"] = fill((H,), S_DTBIAS, K_NORMAL, 0.0, 0.5, "f32", s)
     nseq = wl.nseq if wl.kind == "varlen" else b
     if wl.h0_std > 0:
         d["h0"] = unit((nseq, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32")
     if wl.carry:
-        d["prev_B"] = unit((nseq, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, row_len=N)
+        d["prev_B"] = unit((nseq, H, R, N), S_PREVB, K_NORMAL, 0.0, 2.0, dt_) if wl.prologue else \
+            unit((nseq, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, row_len=N)
         d["prev_x"] = unit((nseq, H, R, P), S_PREVX, K_NORMAL, 0.0, 1.0, dt_)
     return d
 
@@ -294,9 +311,12 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
 
     d = {
         "x": step_fill((b, H, R, P), S_X, K_NORMAL, 0.0, 1.0),
-        "B": step_fill((b, G, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
-        "C": step_fill((b, G, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
-        "dt": step_fill((b, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
+        "B": step_fill((b, G, R, N), S_B, K_NORMAL, 0.0, 2.0) if wl.prologue else
+        step_fill((b, G, R, N), S_B, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "C": step_fill((b, G, R, N), S_C, K_NORMAL, 0.0, 2.0) if wl.prologue else
+        step_fill((b, G, R, N), S_C, K_NORMAL_RMS, RMS_EPS, 0.0, row_len=N),
+        "dt": step_fill((b, H), S_DT, K_NORMAL, wl.dt_shift, 1.0) if wl.prologue else
+        step_fill((b, H), S_DT, K_SOFTPLUS, wl.dt_shift, 0.0),
         "lam": step_fill((b, H), S_LAM, K_SIGMOID, 0.0, 0.0),
         "theta": step_fill((b, H, N // 2), S_THETA, K_UNIFORM, 0.0, np.pi),
         "A": fill((H,), S_A, K_NEG_EXP, 0.0, 0.5, "f32", s),
@@ -306,12 +326,15 @@ def decode_inputs(wl: Workload, steps: int | None = None, first_step: int = 0) -
         d["theta"] = None
     if wl.euler:
         d["lam"] = None
+    if wl.prologue:
+        d["dt_bias"] = fill((H,), S_DTBIAS, K_NORMAL, 0.0, 0.5, "f32", s)
     if wl.h0_std > 0:
         d["h0"] = unit((b, H, N // 2, P, 2), S_H0, K_NORMAL, 0.0, wl.h0_std, "f32")
     else:
         d["h0"] = np.zeros((b, H, N // 2, P, 2), np.float32)
     if wl.carry:
-        d["prev_B"] = unit((b, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, row_len=N)
+        d["prev_B"] = unit((b, H, R, N), S_PREVB, K_NORMAL, 0.0, 2.0, dt_) if wl.prologue else \
+            unit((b, H, R, N), S_PREVB, K_NORMAL_RMS, RMS_EPS, 0.0, dt_, row_len=N)
         d["prev_x"] = unit((b, H, R, P), S_PREVX, K_NORMAL, 0.0, 1.0, dt_)
     else:
         z = np.uint16 if dt_ == "bf16" else np.float32

@@ -35,14 +35,16 @@ def assert_close(got, ref, tol, what):
     return e
 
 
-def prefill_gpu(inp: dict, wl, *, state=None, cu=None, algo=m3.M3_ALGO_AUTO, chunk=0):
+def prefill_gpu(inp: dict, wl, *, state=None, cu=None, algo=m3.M3_ALGO_AUTO, chunk=0, y_dtype=torch.float32,
+                prologue=0):
     """Run m3_scan_prefill on device copies of ``inp``; returns y (torch)."""
     t = {k: dev(v) for k, v in inp.items() if k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
     b, L, H, R, P = inp["x"].shape
-    y = torch.empty((b, L, H, R, P), dtype=torch.float32, device="cuda")
+    y = torch.empty((b, L, H, R, P), dtype=y_dtype, device="cuda")
     cu_t = None if cu is None else torch.from_numpy(np.asarray(cu, np.int32)).cuda()
     m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                       state=state, cu_seqlens=cu_t, algo=algo, chunk=chunk)
+                       state=state, cu_seqlens=cu_t, algo=algo, chunk=chunk, prologue=prologue,
+                       dt_bias=dev(inp.get("dt_bias")) if prologue else None)
     return y
 
 
