@@ -4,6 +4,7 @@ transposed operand, a stale carry) and check that some pin fails."""
 import os
 import shutil
 
+import numpy as np
 import pytest
 
 import oracle
@@ -58,3 +59,61 @@ def test_unmutated_passes_all():
     lib = oracle.load()
     for pin in pins.ALL_PINS:
         pin(lib)
+
+
+# The fused prologue lives in the oracle's Python wrapper: plant slips there
+# (monkeypatched for one test) and check that a prologue pin fails.
+def _prologue_pins():
+    import test_oracle_prologue as t
+
+    return [t.test_softplus_closed_forms, t.test_softplus_matches_the_generators_formula,
+            t.test_bias_enters_before_softplus, t.test_rms_normalize_definition,
+            lambda: t.test_norm_undoes_a_positive_scale_of_each_row(2),
+            t.test_prologue_on_already_normalised_inputs_is_the_plain_scan]
+
+
+def _apply_prologue_variant(bias_after=False, skip_prev_B=False):
+    def f(inp, dtype, *, dt_softplus=False, bc_norm=False, dt_bias=None):
+        out = {k: (v if (v is None or k in ("A", "D", "h0", "dt_bias")) else oracle._widen(v, dtype))
+               for k, v in inp.items()}
+        bias = 0.0 if dt_bias is None else np.asarray(dt_bias, np.float64)
+        if dt_softplus:
+            out["dt"] = oracle.softplus(out["dt"]) + bias if bias_after else oracle.softplus(out["dt"] + bias)
+        if bc_norm:
+            for k in ("B", "C") if skip_prev_B else ("B", "C", "prev_B"):
+                if out.get(k) is not None:
+                    out[k] = oracle.rms_normalize(out[k])
+        return out
+    return f
+
+
+def _rms(axis=-1, sqrt=True, mean=True):
+    def f(a, eps=1e-6):
+        a = np.asarray(a, np.float64)
+        ms = (np.mean if mean else np.sum)(a * a, axis=axis, keepdims=True) + eps
+        return a / (np.sqrt(ms) if sqrt else ms)
+    return f
+
+
+PROLOGUE_MUTANTS = {
+    "rms_sum_not_mean": ("rms_normalize", _rms(mean=False)),
+    "rms_over_wrong_axis": ("rms_normalize", _rms(axis=-2)),
+    "rms_without_sqrt": ("rms_normalize", _rms(sqrt=False)),
+    "softplus_without_abs": ("softplus", lambda z: np.maximum(z, 0.0) + np.log1p(np.exp(-np.asarray(z, float)))),
+    "softplus_as_relu": ("softplus", lambda z: np.maximum(np.asarray(z, float), 0.0)),
+    "bias_after_softplus": ("apply_prologue", _apply_prologue_variant(bias_after=True)),
+    "carried_B_not_normalised": ("apply_prologue", _apply_prologue_variant(skip_prev_B=True)),
+}
+
+
+@pytest.mark.parametrize("name", list(PROLOGUE_MUTANTS))
+def test_prologue_mutant_is_caught(monkeypatch, name):
+    attr, fn = PROLOGUE_MUTANTS[name]
+    monkeypatch.setattr(oracle, attr, fn)
+    failed = []
+    for pin in _prologue_pins():
+        try:
+            pin()
+        except AssertionError:
+            failed.append(getattr(pin, "__name__", "pin"))
+    assert failed, f"no prologue pin caught {name}"

@@ -32,6 +32,18 @@ def test_softplus_matches_the_generators_formula():
         assert np.allclose(oracle.softplus(raw), gen, rtol=1e-14, atol=0)
 
 
+def test_bias_enters_before_softplus():
+    """dt_bias is added to the pre-activation: raw draws N(0, 1) with a
+    per-head bias equal to the generator's shift give the generator's own
+    softplus(N(0, 1) + shift), head by head."""
+    shifts = np.array([-4.0, -1.0, 2.0])
+    raw = synth.fill((2, 50, 3), synth.S_DT, synth.K_NORMAL, 0.0, 1.0, "f64")
+    out = oracle.apply_prologue({"dt": raw}, "f64", dt_softplus=True, dt_bias=shifts)["dt"]
+    for h, sh in enumerate(shifts):
+        gen = synth.fill((2, 50, 3), synth.S_DT, synth.K_SOFTPLUS, sh, 0.0, "f64")
+        assert np.allclose(out[..., h], gen[..., h], rtol=1e-14, atol=0)
+
+
 def test_rms_normalize_definition():
     rng = np.random.default_rng(0)
     a = rng.normal(0, 3, (5, 7, 64)) * rng.uniform(0.1, 10, (5, 7, 1))

@@ -36,24 +36,27 @@ def _global_varlen(nseq):
     return wl
 
 
+@pytest.mark.parametrize("variant", [{}, dict(ngroups=1, prologue=True)], ids=["per_head", "grouped_raw"])
 @pytest.mark.parametrize("world", [2, 3])
-def test_prefill_shards_concatenate_to_global(world):
-    glob = synth.prefill_inputs(_prefill_wl(2 * world))
-    parts = [synth.prefill_inputs(synth.shard(_prefill_wl(2), r, world)) for r in range(world)]
+def test_prefill_shards_concatenate_to_global(world, variant):
+    glob = synth.prefill_inputs(synth.scaled(_prefill_wl(2 * world), **variant))
+    parts = [synth.prefill_inputs(synth.shard(synth.scaled(_prefill_wl(2), **variant), r, world))
+             for r in range(world)]
     for k in glob:
-        if k in ("A", "D"):
+        if k in ("A", "D", "dt_bias"):  # per head: the same on every rank
             for p in parts:
                 assert np.array_equal(p[k], glob[k]), k
         else:
             assert np.array_equal(np.concatenate([p[k] for p in parts], 0), glob[k]), k
 
 
-def test_decode_shards_concatenate_to_global():
-    base = synth.Workload("t", "decode", 2, 0, 3, 8, 16, 4, "bf16", h0_std=0.1, carry=True)
+@pytest.mark.parametrize("variant", [{}, dict(ngroups=1, prologue=True)], ids=["per_head", "grouped_raw"])
+def test_decode_shards_concatenate_to_global(variant):
+    base = synth.Workload("t", "decode", 2, 0, 3, 8, 16, 4, "bf16", h0_std=0.1, carry=True, **variant)
     glob = synth.decode_inputs(synth.scaled(base, batch=4), steps=5, first_step=3)
     parts = [synth.decode_inputs(synth.shard(base, r, 2), steps=5, first_step=3) for r in range(2)]
     for k in glob:
-        if k in ("A", "D"):
+        if k in ("A", "D", "dt_bias"):
             assert all(np.array_equal(p[k], glob[k]) for p in parts), k
         elif k in ("h0", "prev_B", "prev_x"):
             assert np.array_equal(np.concatenate([p[k] for p in parts], 0), glob[k]), k
