@@ -48,6 +48,8 @@ struct DecodeParams {
 };
 
 // R is the rank when known at compile time; R == 0 reads it from p.R (<= 8).
+// YB: y is written in bf16 (else f32); a template flag, so that the f32
+// kernel is compiled exactly as without the option.
 //
 // The unit's state (K*P complex f32, 16-32 KB) moves HBM -> shared memory
 // with one bulk asynchronous copy (completing on an mbarrier) issued before
@@ -58,7 +60,7 @@ struct DecodeParams {
 // float4 per pair) read with 128-bit broadcast loads (every lane of a warp
 // works on the same k); each thread keeps the x values of its two p columns
 // in registers.
-template <typename T, int ITEMS, int R_>
+template <typename T, int ITEMS, int R_, bool YB>
 __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) {
   using namespace umma;
   extern __shared__ float4 smem4[];
@@ -244,11 +246,12 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
     bulk_commit();
   }
   const int64_t y0 = (int64_t)unit * R * P;
-  for (int i = tid; i < R * P; i += blockDim.x) {
+  auto y_at = [&](int i) {
     float sum = 0.f;
     for (int g = 0; g < KG; ++g) sum += red[g * R * P + i];
-    st_y(p.y, y0 + i, fmaf(D, xs[i], sum), p.ybf);
-  }
+    return fmaf(D, xs[i], sum);
+  };
+  for (int i = tid; i < R * P; i += blockDim.x) st_y(p.y, y0 + i, y_at(i), YB);
   if (tid == 0) bulk_wait_read_all();  // shared memory must outlive the copy's reads
 }
 

@@ -43,29 +43,40 @@ m3_status launch_status() {
 
 // ---------------------------------------------------------------- decode
 
-template <typename T, int ITEMS>
+template <typename T, int ITEMS, bool YB>
 m3_status decode_rank(const m3::DecodeParams& p, int threads, size_t smem, int units,
                       cudaStream_t s) {
   switch (p.R) {
 #define M3_DEC(RR)                                                                             \
   case RR:                                                                                     \
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(m3::decode_step_kernel<T, ITEMS, RR>,          \
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(m3::decode_step_kernel<T, ITEMS, RR, YB>,      \
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                                                  (int)smem) != cudaSuccess)                     \
       return M3_ERR_CUDA;                                                                      \
-    m3::decode_step_kernel<T, ITEMS, RR><<<units, threads, smem, s>>>(p);                      \
+    m3::decode_step_kernel<T, ITEMS, RR, YB><<<units, threads, smem, s>>>(p);                  \
     return launch_status();
     M3_DEC(1) M3_DEC(4)
 #undef M3_DEC
     default:
       if (p.R > 8) return M3_ERR_UNSUPPORTED;
-      if (smem > 48 * 1024 && cudaFuncSetAttribute(m3::decode_step_kernel<T, ITEMS, 0>,
+      if (smem > 48 * 1024 && cudaFuncSetAttribute(m3::decode_step_kernel<T, ITEMS, 0, YB>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)smem) != cudaSuccess)
         return M3_ERR_CUDA;
-      m3::decode_step_kernel<T, ITEMS, 0><<<units, threads, smem, s>>>(p);
+      m3::decode_step_kernel<T, ITEMS, 0, YB><<<units, threads, smem, s>>>(p);
       return launch_status();
   }
+}
+
+template <typename T, bool YB>
+m3_status decode_items(const m3::DecodeParams& p, int items, int threads, size_t smem, int units,
+                       cudaStream_t s) {
+  if (items <= 1) return decode_rank<T, 1, YB>(p, threads, smem, units, s);
+  if (items <= 2) return decode_rank<T, 2, YB>(p, threads, smem, units, s);
+  if (items <= 4) return decode_rank<T, 4, YB>(p, threads, smem, units, s);
+  if (items <= 8) return decode_rank<T, 8, YB>(p, threads, smem, units, s);
+  if (items <= 16) return decode_rank<T, 16, YB>(p, threads, smem, units, s);
+  return M3_ERR_UNSUPPORTED;
 }
 
 template <typename T>
@@ -96,12 +107,8 @@ m3_status decode_launch(m3::DecodeParams p, int units, cudaStream_t s) {
   const size_t smem = sizeof(float4) * p.K * (p.PP + kw) + sizeof(float) * (2 * p.R * p.P + kg * p.R * p.P) +
                       (p.bulk ? raw + 16 : 0);
   if (smem > 200 * 1024) return M3_ERR_UNSUPPORTED;
-  if (items <= 1) return decode_rank<T, 1>(p, threads, smem, units, s);
-  if (items <= 2) return decode_rank<T, 2>(p, threads, smem, units, s);
-  if (items <= 4) return decode_rank<T, 4>(p, threads, smem, units, s);
-  if (items <= 8) return decode_rank<T, 8>(p, threads, smem, units, s);
-  if (items <= 16) return decode_rank<T, 16>(p, threads, smem, units, s);
-  return M3_ERR_UNSUPPORTED;
+  return p.ybf ? decode_items<T, true>(p, items, threads, smem, units, s)
+               : decode_items<T, false>(p, items, threads, smem, units, s);
 }
 
 // ---------------------------------------------------------------- recurrent prefill
