@@ -57,3 +57,33 @@ def test_host_argument_checks_without_gpu():
     assert lib.m3_scan_prefill(ctypes.byref(a), None, None) == m3.M3_ERR_INVALID_ARG
     assert lib.m3_state_view(None, None) == m3.M3_ERR_INVALID_ARG
     assert lib.m3_state_free(None) == m3.M3_OK
+
+
+def _c_layout(tmp_path, structs):
+    """sizeof and offsetof of each field, from the C compiler on the header."""
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "m3scan.h"', "int main(void) {"]
+    for st, fields in structs.items():
+        lines.append(f'  printf("{st} %zu\\n", sizeof({st}));')
+        for f in fields:
+            lines.append(f'  printf("{st}.{f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    import subprocess
+
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)])
+    out = subprocess.check_output([str(exe)], text=True)
+    return dict((k, int(v)) for k, v in (ln.split() for ln in out.splitlines()))
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """The ctypes argument structs the binding passes have the header's
+    size and field offsets (a mismatch would hand the library garbage)."""
+    structs = {"m3_dims": m3.m3_dims, "m3_state_ptrs": m3.m3_state_ptrs,
+               "m3_prefill_args": m3.m3_prefill_args, "m3_decode_args": m3.m3_decode_args}
+    layout = _c_layout(tmp_path, {name: [f for f, _ in cls._fields_] for name, cls in structs.items()})
+    for name, cls in structs.items():
+        assert layout[name] == ctypes.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert layout[f"{name}.{f}"] == getattr(cls, f).offset, f"{name}.{f}"
