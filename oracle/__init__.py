@@ -6,7 +6,8 @@ shares no code with it.
 
 ``m3_oracle.c`` walks the recurrence token by token in complex double (see
 its header for the equations and the readings taken where the pages are
-silent).  This wrapper only builds the table of units (which (sequence,
+silent).  ``backward.py`` is the exact gradient of that forward pass, and
+``apply_prologue`` the fused prologue (softplus of dt, RMS norm of B and C).  This wrapper only builds the table of units (which (sequence,
 head) pairs to walk, and where their tokens live) and converts arrays.
 """
 from __future__ import annotations
@@ -254,3 +255,7 @@ def _widen(a, dtype):
     if dtype == "bf16" and a.dtype == np.uint16:
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return a.astype(np.float64)
+
+
+# the backward pass (gradients of the forward above), for training parity cases
+from .backward import prefill_backward, unit_backward  # noqa: E402,F401
