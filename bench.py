@@ -15,6 +15,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -78,14 +79,22 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src: str) -> str:
+    """C/C++/CUDA source without comments, blank lines or trailing spaces:
+    an edit to a comment leaves the compiled kernel, so the hash, alone."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+
+
 def kernel_source_hash(kind):
-    """Hash of the sources a kernel is built from: a committed DRAM-traffic
-    figure counts only while it matches."""
+    """Hash of the code a kernel is built from (comments excluded): a
+    committed DRAM-traffic figure counts only while it matches."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
         path = os.path.join(ROOT, rel if rel.startswith("include") else os.path.join(PKG, rel))
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

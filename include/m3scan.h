@@ -38,8 +38,9 @@
  *     previous-token term).  With both NULL the scan is the first-order real
  *     SSM of Mamba-2 with N states, on the same layouts.
  *   - Floating point: inputs are f32 or bf16 (in_dtype); dt, lam and theta
- *     share that type; A, D, y and the state are f32; all arithmetic is f32
- *     (tensor-core products take bf16 operands with f32 accumulation).
+ *     share that type; A, D, dt_bias and the state are f32; y is f32 or, on
+ *     request, bf16 (y_dtype); all arithmetic is f32 (tensor-core products
+ *     take f16 hi/lo operand pairs with f32 accumulation).
  */
 #ifndef M3SCAN_H
 #define M3SCAN_H
@@ -127,9 +128,10 @@ typedef struct m3_prefill_args {
   int32_t chunk;  /* tokens per chunk for M3_ALGO_CHUNKED; 0 = the kernel's default    */
   int32_t algo;   /* m3_algo                                                            */
   const void* x;     /* [batch][L][H][R][P]   in_dtype */
-  const void* B;     /* [batch][L][H][R][N]   in_dtype */
-  const void* C;     /* [batch][L][H][R][N]   in_dtype */
-  const void* dt;    /* [batch][L][H]         in_dtype, > 0 */
+  const void* B;     /* [batch][L][G][R][N]   in_dtype; G = ngroups (H by default) */
+  const void* C;     /* [batch][L][G][R][N]   in_dtype */
+  const void* dt;    /* [batch][L][H]         in_dtype, > 0 (the pre-activation under
+                                                 M3_PRO_DT_SOFTPLUS: any value) */
   const void* lam;   /* [batch][L][H]         in_dtype, in [0, 1]; NULL: lam = 1 */
   const void* theta; /* [batch][L][H][N/2]    in_dtype; NULL: theta = 0        */
   const float* A;    /* [H] f32, < 0 */
@@ -153,8 +155,8 @@ typedef struct m3_prefill_args {
 typedef struct m3_decode_args {
   m3_dims dims;
   const void* x;     /* [batch][H][R][P] in_dtype */
-  const void* B;     /* [batch][H][R][N] in_dtype */
-  const void* C;     /* [batch][H][R][N] in_dtype */
+  const void* B;     /* [batch][G][R][N] in_dtype; G = ngroups (H by default) */
+  const void* C;     /* [batch][G][R][N] in_dtype */
   const void* dt;    /* [batch][H]       in_dtype */
   const void* lam;   /* [batch][H]       in_dtype; NULL: lam = 1   */
   const void* theta; /* [batch][H][N/2]  in_dtype; NULL: theta = 0 */
@@ -189,8 +191,10 @@ M3_API m3_status m3_state_view(const m3_state* st, m3_state_ptrs* out);
  * is nseq.  With cu_seqlens (batch must be 1), each packed sequence
  * [cu[s], cu[s+1]) is its own unit: h and the carry restart at every
  * boundary (from the state slot s when st is given).
- * Errors: M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED (algo CHUNKED on a shape
- * or dtype without a chunked kernel), M3_ERR_CUDA.
+ * Errors: M3_ERR_INVALID_ARG (also: ngroups < 0 or not dividing H, an
+ * unknown y_dtype, unknown prologue bits), M3_ERR_UNSUPPORTED (algo CHUNKED
+ * on a shape or dtype without a chunked kernel, or with theta NULL and
+ * M3_PRO_BC_NORM), M3_ERR_CUDA.
  */
 M3_API m3_status m3_scan_prefill(const m3_prefill_args* args, m3_state* st, void* stream);
 
@@ -221,7 +225,8 @@ M3_API m3_status m3_scan_prefill_noalloc(const m3_prefill_args* args, m3_state* 
 /*
  * Decode step: advance every sequence of st by one token, write y, and
  * replace the carry with this token's (B, x).  args->dims must equal st's.
- * Errors: M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA.
+ * Errors: M3_ERR_INVALID_ARG (as for the prefill), M3_ERR_UNSUPPORTED,
+ * M3_ERR_CUDA.
  */
 M3_API m3_status m3_decode_step(const m3_decode_args* args, m3_state* st, void* stream);
 
