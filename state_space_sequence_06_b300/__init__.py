@@ -22,7 +22,7 @@ M3_ALGO_AUTO, M3_ALGO_RECURRENT, M3_ALGO_CHUNKED = 0, 1, 2
 M3_PRO_DT_SOFTPLUS, M3_PRO_BC_NORM = 1, 2
 
 SYMBOLS = ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
-           "m3_decode_step", "m3_device_status", "m3_status_string")
+           "m3_decode_step", "m3_device_status", "m3_status_string", "m3_scan_prefill_backward")
 
 
 class M3Error(RuntimeError):
@@ -56,6 +56,14 @@ class m3_decode_args(ctypes.Structure):
          ("dt_bias", ctypes.c_void_p)]
 
 
+class m3_backward_args(ctypes.Structure):
+    _fields_ = [("dims", m3_dims), ("seqlen", ctypes.c_int64)] + \
+        [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "h0", "prev_B", "prev_x",
+                                        "dy", "dh_final", "dx", "dB", "dC", "ddt", "dlam", "dtheta", "dA", "dD",
+                                        "dh0", "dprev_B", "dprev_x")] + \
+        [("ngroups", ctypes.c_int32)]
+
+
 _lib = None
 
 
@@ -74,9 +82,10 @@ def load_library(path: str = LIB_PATH):
     lib.m3_scan_prefill.argtypes = [ctypes.POINTER(m3_prefill_args), vp, vp]
     lib.m3_scan_prefill_noalloc.argtypes = [ctypes.POINTER(m3_prefill_args), vp, vp]
     lib.m3_decode_step.argtypes = [ctypes.POINTER(m3_decode_args), vp, vp]
+    lib.m3_scan_prefill_backward.argtypes = [ctypes.POINTER(m3_backward_args), vp]
     lib.m3_device_status.argtypes = [vp]
     for f in ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
-              "m3_scan_prefill_noalloc", "m3_decode_step", "m3_device_status"):
+              "m3_scan_prefill_noalloc", "m3_decode_step", "m3_device_status", "m3_scan_prefill_backward"):
         getattr(lib, f).restype = ctypes.c_int
     lib.m3_status_string.argtypes = [ctypes.c_int]
     lib.m3_status_string.restype = ctypes.c_char_p
@@ -230,6 +239,35 @@ def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None, 
     a.A, a.D, a.y = _ptr(A), _ptr(D), _ptr(y)
     _check(load_library().m3_decode_step(ctypes.byref(a), state.handle, _stream(stream)),
            "m3_decode_step")
+
+
+def m3_scan_prefill_backward(x, B, C, dt, lam, theta, A, D, dy, *, h0=None, prev_B=None, prev_x=None,
+                             dh_final=None, stream=None) -> dict:
+    """Gradients of a loss with respect to every prefill input, given dy =
+    dL/dy [b][L][H][R][P] f32 (and dh_final = dL/dh_final [b][H][N/2][P][2]).
+    Inputs as for m3_scan_prefill (fixed-length batch); h0 [b][H][N/2][P][2]
+    f32, prev_B / prev_x the carry.  Returns f32 CUDA tensors dx, dB, dC,
+    ddt, dlam, dtheta, dA, dD, dh0, dprev_B, dprev_x in the inputs' layouts
+    (allocated here; the kernel is the library's)."""
+    b, L, H, R, P = x.shape
+    N = B.shape[-1]
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = dict(dx=torch.empty(x.shape, **f32), dB=torch.empty(B.shape, **f32), dC=torch.empty(C.shape, **f32),
+               ddt=torch.empty(dt.shape, **f32), dlam=torch.empty(dt.shape, **f32),
+               dtheta=torch.empty(dt.shape + (N // 2,), **f32), dA=torch.empty(H, **f32),
+               dD=torch.empty(H, **f32), dh0=torch.empty((b, H, N // 2, P, 2), **f32),
+               dprev_B=torch.empty((b, H, R, N), **f32), dprev_x=torch.empty((b, H, R, P), **f32))
+    a = m3_backward_args()
+    a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
+    a.seqlen, a.ngroups = L, B.shape[2]
+    for name, t in (("x", x), ("B", B), ("C", C), ("dt", dt), ("lam", lam), ("theta", theta), ("A", A),
+                    ("D", D), ("h0", h0), ("prev_B", prev_B), ("prev_x", prev_x), ("dy", dy),
+                    ("dh_final", dh_final)):
+        setattr(a, name, _ptr(t))
+    for name, t in out.items():
+        setattr(a, name, _ptr(t))
+    _check(load_library().m3_scan_prefill_backward(ctypes.byref(a), _stream(stream)), "m3_scan_prefill_backward")
+    return out
 
 
 def m3_device_status(stream=None) -> int:

@@ -43,7 +43,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     nvcc = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-shared", "-o", tmp,
-           os.path.join(CSRC, "m3scan.cu")]
+           os.path.join(CSRC, "m3scan.cu"), os.path.join(CSRC, "backward.cu")]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.check_call(cmd)

@@ -61,7 +61,8 @@ def test_host_argument_checks_without_gpu():
 
 def _c_layout(tmp_path, structs):
     """sizeof and offsetof of each field, from the C compiler on the header."""
-    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "m3scan.h"', "int main(void) {"]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "m3scan.h"', '#include "m3scan_backward.h"',
+             "int main(void) {"]
     for st, fields in structs.items():
         lines.append(f'  printf("{st} %zu\\n", sizeof({st}));')
         for f in fields:
@@ -81,7 +82,8 @@ def test_binding_structs_match_the_header_layout(tmp_path):
     """The ctypes argument structs the binding passes have the header's
     size and field offsets (a mismatch would hand the library garbage)."""
     structs = {"m3_dims": m3.m3_dims, "m3_state_ptrs": m3.m3_state_ptrs,
-               "m3_prefill_args": m3.m3_prefill_args, "m3_decode_args": m3.m3_decode_args}
+               "m3_prefill_args": m3.m3_prefill_args, "m3_decode_args": m3.m3_decode_args,
+               "m3_backward_args": m3.m3_backward_args}
     layout = _c_layout(tmp_path, {name: [f for f, _ in cls._fields_] for name, cls in structs.items()})
     for name, cls in structs.items():
         assert layout[name] == ctypes.sizeof(cls), name
