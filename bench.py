@@ -476,6 +476,8 @@ def main():
     # sequences) of a global batch world times the workload's
     wls = {k: synth.shard(w, rank, world) for k, w in wls.items()}
     wl = wls[args.workload]
+    if wl.backward:  # a line of its own, run only by name
+        return run_backward(wl, args, m3, torch, dist, world, rank, local, stream)
 
     head = measure(wl, args, m3, torch, dist, world, local, stream, headline=True)
     others = []
@@ -522,6 +524,75 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
+    """Time m3_scan_prefill_backward (the token-serial reference kernel) on
+    a prefill workload with a seeded dL/dy and dL/dh_final; one pass = every
+    gradient of the batch.  Algorithmic bytes: the forward inputs and dL/dy
+    read once, every gradient written once (the kernel's own history
+    scratch is not counted).  Unit 0's dx and ddt are checked against the
+    oracle's adjoint."""
+    import oracle
+
+    H, P, N, R, L, b = wl.nheads, wl.headdim, wl.dstate, wl.rank, wl.seqlen, wl.batch
+    inp = synth.prefill_inputs(wl)
+    rng = np.random.default_rng(0)
+    dy = rng.normal(size=(b, L, H, R, P)).astype(np.float32)
+    dhf = rng.normal(size=(b, H, N // 2, P, 2)).astype(np.float32)
+    t = {k: dev_tensor(torch, inp[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "h0", "prev_B",
+                                                "prev_x")}
+    dy_d, dhf_d = dev_tensor(torch, dy), dev_tensor(torch, dhf)
+
+    def once():
+        return m3.m3_scan_prefill_backward(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"],
+                                           dy_d, h0=t["h0"], prev_B=t["prev_B"], prev_x=t["prev_x"],
+                                           dh_final=dhf_d)
+
+    for _ in range(args.warmup):
+        out = once()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            out = once()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = max_over_ranks(torch, dist, world, e0.elapsed_time(e1), "cuda")
+    status = m3.m3_device_status()
+    # parity of unit 0 (sequence 0, head 0) against the adjoint oracle
+    w = lambda k: oracle._widen(inp[k], wl.dtype)
+    g = 0  # head 0 reads group 0
+    _, _, ref = oracle.unit_backward(w("x")[0, :, 0], w("B")[0, :, g], w("C")[0, :, g], w("dt")[0, :, 0],
+                                     w("lam")[0, :, 0], w("theta")[0, :, 0], float(inp["A"][0]),
+                                     float(inp["D"][0]), inp["h0"][0, 0, ..., 0] + 1j * inp["h0"][0, 0, ..., 1],
+                                     w("prev_B")[0, 0], w("prev_x")[0, 0], dy[0, :, 0].astype(np.float64),
+                                     dhf[0, 0, ..., 0] + 1j * dhf[0, 0, ..., 1])
+    err = {}
+    for gk, rk in (("dx", "x"), ("ddt", "dt")):
+        got = out[gk][0, :, 0].double().cpu().numpy()
+        err[gk] = float(np.max(np.abs(got - ref[rk])) / max(np.sqrt(np.mean(ref[rk] ** 2)), 1e-30))
+    isz = 2 if wl.dtype == "bf16" else 4
+    th = b * L * H
+    in_bytes = th * (R * P + 2 * R * N + 2 + N // 2) * isz + th * R * P * 4
+    out_bytes = th * (R * P + 2 * R * N + 2 + N // 2) * 4
+    byt = in_bytes + out_bytes
+    per_ms = total_ms / args.steps
+    hbm_peak, _, peak_src = peaks()
+    achieved = byt / (per_ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "Mamba-3 scan backward tokens/s (token-serial reference kernel)",
+            "value": b * L * world / (per_ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(config_of(wl), **{"pass": "backward (all gradients, f32)"}),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": byt},
+            "gpu_launches": args.steps, "device_status": status, "clocks": clk.summary(),
+            "parity": {"unit": 0, "max_err_over_rms": err}}), flush=True)
 
 
 def sampled_parity(wl, m3, t, y, st, cu, algo):

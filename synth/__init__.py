@@ -125,6 +125,7 @@ class Workload:
     # with a per-head bias N(0, 0.5), B and C (and the carried B) N(0, 2^2)
     # without row normalisation
     prologue: bool = False
+    backward: bool = False  # a training-pass workload: the backward of this prefill (timed by name only)
     cu_seqlens: np.ndarray | None = field(default=None, repr=False)
     # shard of a global problem: this shard's `batch` sequences (varlen:
     # `nseq` sequences) are number shard_index*batch.. of a global batch of
@@ -180,6 +181,9 @@ def workloads() -> dict:
         # the same SISO prefill from raw inputs: dt before softplus, B and C before the RMS norm
         "siso_prologue_b8_l4096": Workload("siso_prologue_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16",
                                            chunk=64, prologue=True),
+        # the backward pass of a prefill (token-serial reference kernel), batch 2, L 1024
+        "backward_siso_b2_l1024": Workload("backward_siso_b2_l1024", "prefill", 2, 1024, 32, 64, 128, 1, "bf16",
+                                           h0_std=0.1, carry=True, backward=True),
         "varlen_16": Workload(
             "varlen_16", "varlen", 1, 0, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0,
             nseq=16, len_lo=256, len_hi=8192,
