@@ -17,7 +17,6 @@ import json
 import os
 import re
 import statistics
-import subprocess
 import sys
 import time
 

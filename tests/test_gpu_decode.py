@@ -6,7 +6,7 @@ import torch
 import oracle
 import state_space_sequence_06_b300 as m3
 import synth
-from gpu_util import TOL, assert_close, dev, state_for, to_np
+from gpu_util import TOL, dev, state_for, to_np
 
 pytestmark = pytest.mark.gpu
 

@@ -2,7 +2,6 @@
 the oracle's source (a dropped term, a wrong sign, a wrong index, a
 transposed operand, a stale carry) and check that some pin fails."""
 import os
-import shutil
 
 import numpy as np
 import pytest
