@@ -507,22 +507,27 @@ def main():
             cpu = {"error": repr(e)[:200]}
 
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": head["dtype"],
-            "data": "synthetic (seeded generator; shapes of the pages' 1.5B-scale workloads)",
-            "config": dict(head["config"], algo=args.algo,
-                           l2=("inputs larger than L2 (%.2f GB per pass vs 126 MB L2)"
-                               % (head["roofline"]["algorithmic_bytes_per_launch"] / 1e9)),
-                           parallelism=f"replicas over independent units x{world}"),
-            "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head.get("e2e"),
-            "gpu_launches": head["gpu_launches"], "device_status": head["device_status"],
-            "clocks": head["clocks"], "parity": head["parity"], "workloads": others,
-        }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(contract_line(head, cpu, others, args, world)), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def contract_line(head, cpu, others, args, world):
+    """The one JSON line of a run: the headline measurement `head` (from
+    measure()), the CPU oracle baseline and the other workloads' lines."""
+    return {
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": head["dtype"],
+        "data": "synthetic (seeded generator; shapes of the pages' 1.5B-scale workloads)",
+        "config": dict(head["config"], algo=args.algo,
+                       l2=("inputs larger than L2 (%.2f GB per pass vs 126 MB L2)"
+                           % (head["roofline"]["algorithmic_bytes_per_launch"] / 1e9)),
+                       parallelism=f"replicas over independent units x{world}"),
+        "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head.get("e2e"),
+        "gpu_launches": head["gpu_launches"], "device_status": head["device_status"],
+        "clocks": head["clocks"], "parity": head["parity"], "workloads": others,
+    }
 
 
 def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
