@@ -99,8 +99,62 @@ def unit_backward(x, B, C, dt, lam, theta, A, D, h0, prev_B, prev_x, dy, dh_fina
     return y, hs[-1], g
 
 
+def _sigmoid(z):
+    return 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def _rms_norm_backward(v, dn, eps):
+    """Gradient through n = v / sqrt(mean(v^2) + eps) (rows on the last
+    axis): with s = (mean(v^2) + eps)^(-1/2), dn_i/dv_j = s delta_ij -
+    s^3 v_i v_j / N, so dv = s (dn - n mean(dn * n))."""
+    v = np.asarray(v, np.float64)
+    s = 1.0 / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + eps)
+    n = v * s
+    return s * (dn - n * np.mean(dn * n, axis=-1, keepdims=True))
+
+
+def prologue_backward(inp: dict, grads: dict, dtype: str, *, dt_softplus=False, bc_norm=False, dt_bias=None):
+    """Chain the gradients with respect to the scan's inputs (after the
+    fused prologue) back to the raw inputs the caller passed: dt through
+    softplus(dt + dt_bias[h]) (derivative sigmoid), B, C and the carried
+    prev_B through the RMS norm of each row.  Adds "dt_bias" (summed over
+    batch and tokens per head).  ``inp`` holds the raw inputs."""
+    from . import BC_NORM_EPS, _widen
+
+    g = dict(grads)
+    if dt_softplus:
+        bias = np.zeros(np.shape(inp["dt"])[-1]) if dt_bias is None else np.asarray(dt_bias, np.float64)
+        z = _widen(inp["dt"], dtype) + bias
+        g["dt"] = grads["dt"] * _sigmoid(z)
+        g["dt_bias"] = g["dt"].reshape(-1, z.shape[-1]).sum(axis=0)
+    if bc_norm:
+        for k in ("B", "C", "prev_B"):
+            if inp.get(k) is not None:
+                g[k] = _rms_norm_backward(_widen(inp[k], dtype), grads[k], BC_NORM_EPS)
+    return g
+
+
 def prefill_backward(inp: dict, dy, *, batch, L, H, P, N, R, dtype, h0=None, prev_B=None, prev_x=None,
-                     dh_final=None):
+                     dh_final=None, dt_softplus=False, bc_norm=False, dt_bias=None):
+    """See _prefill_backward.  With dt_softplus / bc_norm the inputs are raw
+    (the fused prologue applies softplus(dt + dt_bias) and the RMS norm of
+    B, C and prev_B rows, as the library's prologue flags do) and the
+    gradients are with respect to them (plus "dt_bias")."""
+    if not (dt_softplus or bc_norm):
+        return _prefill_backward(inp, dy, batch=batch, L=L, H=H, P=P, N=N, R=R, dtype=dtype, h0=h0,
+                                 prev_B=prev_B, prev_x=prev_x, dh_final=dh_final)
+    from . import _widen, apply_prologue
+
+    raw = dict(inp, prev_B=prev_B)
+    post = apply_prologue(raw, dtype, dt_softplus=dt_softplus, bc_norm=bc_norm, dt_bias=dt_bias)
+    y, hf, grads = _prefill_backward(post, dy, batch=batch, L=L, H=H, P=P, N=N, R=R, dtype="f64", h0=h0,
+                                     prev_B=post["prev_B"], prev_x=None if prev_x is None else _widen(prev_x, dtype),
+                                     dh_final=dh_final)
+    return y, hf, prologue_backward(raw, grads, dtype, dt_softplus=dt_softplus, bc_norm=bc_norm, dt_bias=dt_bias)
+
+
+def _prefill_backward(inp: dict, dy, *, batch, L, H, P, N, R, dtype, h0=None, prev_B=None, prev_x=None,
+                      dh_final=None):
     """Gradients of sum(dy * y) + sum(dh_final * h_final) for a fixed-length
     batch (the oracle's layouts: x [b][L][H][R][P], B/C [b][L][G][R][N],
     dt/lam [b][L][H], theta [b][L][H][N/2], A/D [H]; h0 [b][H][N/2][P][2],

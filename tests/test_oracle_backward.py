@@ -103,3 +103,63 @@ def test_backward_mutant_is_caught(monkeypatch, name, find, repl):
     with pytest.raises(AssertionError):
         for R, G in [(1, 4), (2, 2)]:
             test_gradients_match_finite_differences(R, G)
+
+
+def _loss_prologue(inp, st, dims, dy, dh, bias):
+    post = oracle.apply_prologue(dict(inp, prev_B=st["prev_B"]), "f64", dt_softplus=True, bc_norm=True, dt_bias=bias)
+    st2 = dict(st, prev_B=post.pop("prev_B"))
+    y, h, _, _, _ = oracle.prefill(post, **dims, dtype="f64", nthreads=1, **st2)
+    return float(np.sum(dy * y) + np.sum(dh * h.reshape(dh.shape)))
+
+
+@pytest.mark.parametrize("R,G", [(1, 4), (2, 2)])
+def test_prologue_gradients_match_finite_differences(R, G):
+    """With the fused prologue (softplus of dt + dt_bias, RMS norm of B, C
+    and the carried B rows) the gradients are with respect to the raw
+    inputs: central finite differences of the prologue-then-scan forward
+    oracle along a random direction per raw input, dt_bias included."""
+    inp, st, dims, dy, dh = _case(R, G, seed=5)
+    inp = dict(inp, dt=inp["dt"] * 8 - 3)  # pre-activations on both sides of 0
+    bias = np.random.default_rng(9).normal(size=dims["H"]) * 0.5
+    _, _, g = oracle.prefill_backward(inp, dy, **dims, dtype="f64", dh_final=dh, dt_softplus=True, bc_norm=True,
+                                      dt_bias=bias, **st)
+    rng = np.random.default_rng(13)
+    eps = 1e-6
+    for key in ("dt", "B", "C", "prev_B", "x", "dt_bias"):
+        if key == "dt_bias":
+            v = rng.normal(size=bias.shape)
+            fd = (_loss_prologue(inp, st, dims, dy, dh, bias + eps * v)
+                  - _loss_prologue(inp, st, dims, dy, dh, bias - eps * v)) / (2 * eps)
+        else:
+            src = st if key in st else inp
+            v = rng.normal(size=np.shape(src[key]))
+            pl = {k: (w + eps * v if k == key else w) for k, w in src.items()}
+            mi = {k: (w - eps * v if k == key else w) for k, w in src.items()}
+            if key in st:
+                fd = (_loss_prologue(inp, pl, dims, dy, dh, bias) - _loss_prologue(inp, mi, dims, dy, dh, bias)) / (2 * eps)
+            else:
+                fd = (_loss_prologue(pl, st, dims, dy, dh, bias) - _loss_prologue(mi, st, dims, dy, dh, bias)) / (2 * eps)
+        an = float(np.sum(g[key] * v))
+        assert abs(an - fd) <= 1e-6 * max(1.0, abs(fd)), f"{key}: adjoint {an:.9g} vs finite difference {fd:.9g}"
+
+
+def test_rms_norm_backward_slips_are_caught():
+    """The norm's Jacobian pin is sharp: the full chain dv = s (dn - n
+    mean(dn n)) matches the finite difference of B, and dropping its
+    projection term (dv = s dn) misses it by far more than the bound."""
+    from oracle import backward as ob
+
+    inp, st, dims, dy, dh = _case(1, 4, seed=5)
+    bias = np.zeros(dims["H"])
+    post = oracle.apply_prologue(dict(inp, prev_B=st["prev_B"]), "f64", dt_softplus=True, bc_norm=True, dt_bias=bias)
+    post_grads = ob._prefill_backward(post, dy, **dims, dtype="f64", h0=st["h0"], prev_B=post["prev_B"],
+                                      prev_x=st["prev_x"], dh_final=dh)[2]
+    v = np.random.default_rng(1).normal(size=inp["B"].shape)
+    eps = 1e-6
+    fd = (_loss_prologue(dict(inp, B=inp["B"] + eps * v), st, dims, dy, dh, bias)
+          - _loss_prologue(dict(inp, B=inp["B"] - eps * v), st, dims, dy, dh, bias)) / (2 * eps)
+    right = float(np.sum(ob._rms_norm_backward(inp["B"], post_grads["B"], oracle.BC_NORM_EPS) * v))
+    assert abs(right - fd) <= 1e-6 * max(1.0, abs(fd))
+    s = 1.0 / np.sqrt(np.mean(inp["B"] ** 2, axis=-1, keepdims=True) + oracle.BC_NORM_EPS)
+    wrong = float(np.sum(s * post_grads["B"] * v))
+    assert abs(wrong - fd) > 1e-4 * max(1.0, abs(fd))
