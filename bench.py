@@ -33,6 +33,7 @@ PKG = "state_space_sequence_06_b300"
 
 
 def peaks():
+    """HBM GB/s and dense bf16 TFLOP/s (burst: the kernels are timed alone)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
@@ -68,6 +69,32 @@ def workload_bytes(wl) -> dict:
     total = int(round(th * (per_th_in + R * P * ysz))) + state + carry
     return dict(per_unit_of_work=total, unit="pass", inputs=int(round(th * per_th_in)), y=th * R * P * ysz,
                 state=state, carry=carry, per_token_head=per_th_in + R * P * ysz)
+
+
+def contraction_flops(wl) -> dict:
+    """Tensor-core work of one chunked prefill pass.
+
+    ``algorithmic``: the chunked form's contractions per token and head,
+    2QR^2 N (scores C B^T) + 2QR^2 P (intra output S' X) + 2RNP (inter
+    output C^H G') + 2RNP (chunk state B^T W X), for the chunk Q the kernel
+    runs (the quadratic form of the Mamba-2 duality the chunked scan uses).
+    ``issued``: what the kernel actually issues on the tensor cores: every
+    product of a rotated operand, of S' and of W X is a hi/lo pair of f16
+    operands taking three (or two) MMAs; the real-state variant's B and C
+    are exact in f16 and take one."""
+    if wl.kind == "decode" or wl.dtype != "bf16":
+        return {}
+    Q, R, N, P = wl.chunk, wl.rank, wl.dstate, wl.headdim
+    tokens = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
+    th = tokens * wl.nheads
+    per_th = 2 * Q * R * R * N + 2 * Q * R * R * P + 4 * R * N * P
+    rot = 1 if wl.real else 3  # products with a rotated B or C operand
+    # per chunk of MR = QR rows: MMA 1 (MR x MR x N), 2 (MR x P x MR, S' hi/lo),
+    # 3 (MR x P x N, C hi/lo; one product without rotation), 4 (N x P x MR)
+    MR = Q * R
+    issued_chunk = (2 * MR * MR * N * rot + 2 * MR * P * MR * 2 + 2 * MR * P * N * (1 if wl.real else 2)
+                    + 2 * N * P * MR * (2 if wl.real else 3))
+    return {"algorithmic": th * per_th, "issued": th * issued_chunk // Q, "per_token_head": per_th}
 
 
 # the sources each kernel is compiled from (its launcher included)
@@ -329,18 +356,51 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
         y = torch.empty((wl.batch, H, R, P), dtype=torch.bfloat16 if wl.y_bf16 else torch.float32, device="cuda")
         del d
 
-        def step():
+        per_tok = {k: ([None] * T if t[k] is None else [t[k][i] for i in range(T)])
+                   for k in ("x", "B", "C", "dt", "lam", "theta")}
+
+        def reset():
             hv.copy_(h0)  # every pass starts from the same initial state and carry
             pB.copy_(pB0)
             px.copy_(px0)
+
+        def launch(i):
+            m3.m3_decode_step(per_tok["x"][i], per_tok["B"][i], per_tok["C"][i], per_tok["dt"][i],
+                              per_tok["lam"][i], per_tok["theta"][i], t["A"], t["D"], y, st)
+
+        # The T-token pass is captured once as a CUDA graph of the library's
+        # own decode kernels (one launch per token): replaying it removes the
+        # host's per-call cost, which is not the kernel's, from the pass time.
+        reset()
+        for i in range(T):  # eager pass first: lazy module loading and kernel attributes happen here
+            launch(i)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(T):
+                launch(i)
+        torch.cuda.synchronize()
+
+        def step():
+            reset()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            lam, th = t["lam"], t["theta"]
-            for i in range(T):
-                m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], None if lam is None else lam[i],
-                                  None if th is None else th[i], t["A"], t["D"], y, st)
+            graph.replay()
             e1.record(stream)
             ev_pairs.append((e0, e1))
+
+        def per_launch_median_ms():
+            """Median device time of one decode kernel: events around every
+            launch of one eager pass (after the timed region)."""
+            reset()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(T)]
+            torch.cuda.synchronize()
+            for i in range(T):
+                evs[i][0].record(stream)
+                launch(i)
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs)
 
         launches_per_step, units_per_step, unit_name = T, T, "steps/s"
         kernel_key = f"decode_step:{wl.name}"
@@ -365,6 +425,7 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
             e1.record(stream)
             ev_pairs.append((e0, e1))
 
+        per_launch_median_ms = None
         launches_per_step = 1
         units_per_step = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)  # tokens
         unit_name = "tokens/s"
@@ -415,14 +476,33 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
     per_launch_ms = statistics.mean(kern_ms) / launches_per_step
     bytes_per_launch = byt["per_unit_of_work"]  # one prefill pass, or one decode step
     achieved = bytes_per_launch / (per_launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": traffic_for(kernel_key),
+            "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
+            "algorithmic_bytes_per_launch": bytes_per_launch,
+            "kernel_ms_per_launch": per_launch_ms}
+    if per_launch_median_ms is not None:
+        # decode: the pass time / T above includes the gaps between launches
+        # (none to speak of in a graph); this is the kernel alone
+        roof["kernel_ms_per_launch_median_eager"] = per_launch_median_ms()
+    fl = contraction_flops(wl) if path_dtype.startswith("f16x2") else {}
+    if fl:
+        _, tc_peak, tc_src = peaks()
+        sec = per_launch_ms / 1e3
+        ideal_s = bytes_per_launch / (hbm_peak * 1e9)  # the pass at the HBM roofline
+        roof["tensor"] = {
+            "achieved": fl["algorithmic"] / sec / 1e12, "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": fl["algorithmic"] / sec / 1e12 / tc_peak,
+            "flops_per_launch": fl["algorithmic"], "flops_per_token_head": fl["per_token_head"],
+            "issued_mma_flops_per_launch": fl["issued"],
+            "issued_frac": fl["issued"] / sec / 1e12 / tc_peak,
+            "ceiling_frac_at_hbm_roofline": fl["algorithmic"] / ideal_s / 1e12 / tc_peak,
+            "peak_source": tc_src + " (MEASURED_PEAKS.json bf16_tflops, dense bf16 burst)"
+            if tc_src == "measured" else tc_src}
     out = {
         "value": job_rate(units_per_step, args.steps, world, total_ms), "unit": unit_name,
         "ms_per_step": total_ms / args.steps, "dtype": path_dtype,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": traffic_for(kernel_key),
-                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src,
-                     "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "kernel_ms_per_launch": per_launch_ms},
+        "roofline": roof,
         "gpu_launches": launches_per_step * args.steps, "device_status": status,
         "clocks": clk.summary(), "parity": parity, "config": config_of(wl),
     }
@@ -489,12 +569,15 @@ def main():
                 continue
             sargs = argparse.Namespace(**vars(args))
             if wls[name].kind == "decode":
-                sargs.steps = 2  # one step = the whole 1024-token decode loop
+                sargs.steps = 5  # one step = the whole 1024-token decode loop
             r = measure(wls[name], sargs, m3, torch, dist, world, local, stream, headline=False)
             others.append({"workload": name, "value": r["value"], "unit": r["unit"], "ms_per_step": r["ms_per_step"],
                            "dtype": r["dtype"], "roofline_frac": r["roofline"]["frac"],
                            "achieved_gbs": r["roofline"]["achieved"],
                            "kernel_ms_per_launch": r["roofline"]["kernel_ms_per_launch"],
+                           "kernel_ms_per_launch_median_eager":
+                               r["roofline"].get("kernel_ms_per_launch_median_eager"),
+                           "tensor_frac": (r["roofline"].get("tensor") or {}).get("frac"),
                            "gpu_launches": r["gpu_launches"], "device_status": r["device_status"],
                            "clocks": r["clocks"]})
 
@@ -637,38 +720,68 @@ def sampled_parity(wl, m3, t, y, st, cu, algo):
 
 def measure_e2e(wl, m3, torch, t, y, st, cu, algo, args, world):
     """The same metric through the public API from pinned host buffers: each
-    step copies its inputs host -> device, runs the scan and copies y back."""
+    step copies its inputs host -> device, runs the scan and copies y back.
+
+    Steps are pipelined over two sets of device buffers and three streams:
+    the upload of step i + 1 (copy stream) and the download of step i - 1
+    (a second copy stream, the other direction of the link) overlap the scan
+    of step i, ordered by events: a set's inputs are overwritten only after
+    the scan that read them, its y only after the download that read it."""
     if wl.kind == "decode":
         return measure_e2e_decode(wl, m3, torch, t, st, args, world)
     keys = tuple(k for k in ("x", "B", "C", "dt", "lam", "theta") if t[k] is not None)
     host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in keys}
     for k in keys:
         host[k].copy_(t[k])
-    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    sets = [{k: t[k] for k in keys}, {k: torch.empty_like(t[k]) for k in keys}]
+    ys = [y, torch.empty_like(y)]
+    yh = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
     torch.cuda.synchronize()
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
     d2h = y.numel() * y.element_size()
     units = wl.seqlen * (wl.batch if wl.kind == "prefill" else 1)
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    scanned = [None, None]   # set j's last scan done (its inputs read, its y written)
+    fetched = [None, None]   # set j's last download done (its y read)
 
-    def one():
-        for k in keys:
-            t[k].copy_(host[k], non_blocking=True)
-        m3.m3_scan_prefill(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y,
-                           state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk, **prologue_kw(wl, m3, t))
-        yh.copy_(y, non_blocking=True)
+    def one(i):
+        j = i % 2
+        with torch.cuda.stream(up):
+            if scanned[j] is not None:
+                up.wait_event(scanned[j])
+            for k in keys:
+                sets[j][k].copy_(host[k], non_blocking=True)
+            loaded = ev()
+            loaded.record(up)
+        comp.wait_event(loaded)
+        if fetched[j] is not None:
+            comp.wait_event(fetched[j])
+        d = sets[j]
+        m3.m3_scan_prefill(d["x"], d["B"], d["C"], d["dt"], d.get("lam"), d.get("theta"), t["A"], t["D"], ys[j],
+                           state=st, cu_seqlens=cu, algo=algo, chunk=wl.chunk, stream=comp,
+                           **prologue_kw(wl, m3, t))
+        scanned[j] = ev()
+        scanned[j].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(scanned[j])
+            yh[j].copy_(ys[j], non_blocking=True)
+            fetched[j] = ev()
+            fetched[j].record(down)
 
     steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        one()
+    for i in range(2):
+        one(i)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(i)
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
     return {"value": units * steps * world / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
-
+            "d2h_bytes_per_step": d2h,
+            "pipeline": "two buffer sets; upload of step i+1 and download of step i-1 overlap the scan of step i"}
 
 
 def measure_e2e_decode(wl, m3, torch, t, st, args, world):

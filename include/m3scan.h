@@ -171,12 +171,20 @@ typedef struct m3_decode_args {
 
 /*
  * Allocate a state for `dims` and zero it on `stream` (h = 0, no carry).
- * *out receives the handle.  Errors: M3_ERR_INVALID_ARG (bad dims or null
- * out), M3_ERR_ALLOC, M3_ERR_CUDA.
+ * *out receives the handle.  The buffers are stream-ordered allocations on
+ * `stream` (from the device's default memory pool): work on other streams
+ * that uses the state must be ordered after the allocation (an event), and
+ * `stream` must outlive the state.  Errors: M3_ERR_INVALID_ARG (bad dims or
+ * null out), M3_ERR_ALLOC, M3_ERR_CUDA.
  */
 M3_API m3_status m3_state_alloc(const m3_dims* dims, m3_state** out, void* stream);
 
-/* Free a state (synchronises the device first).  NULL is accepted. */
+/*
+ * Free a state.  The buffers are returned in stream order on the stream
+ * given to m3_state_alloc; nothing waits for the device.  Work on other
+ * streams that still uses the state must be ordered before the free on
+ * that stream by the caller.  NULL is accepted.
+ */
 M3_API m3_status m3_state_free(m3_state* st);
 
 /* Fill *out with the state's dims and device pointers. */
@@ -208,12 +216,20 @@ M3_API m3_status m3_scan_prefill(const m3_prefill_args* args, m3_state* st, void
  * (sequence, head) units than the GPU has SMs); this entry point uses a
  * fixed buffer of M3_NOALLOC_SCRATCH_BYTES that is part of the library's
  * module memory instead, and calls no allocating routine.
- *   - The first call on each device looks the buffer's address up (with that
- *     device current) and can fail with M3_ERR_CUDA; make that first call
- *     before any stream capture.
+ *   - The buffer is module memory: CUDA creates it on a device when it
+ *     loads the library's device code there.  Under CUDA's default lazy
+ *     module loading that is the first use of the library on the device,
+ *     not the moment the library is loaded into the process.  The first
+ *     call of this entry point on each device (whatever its arguments)
+ *     looks the buffer's address up with that device current, which loads
+ *     the module and creates the buffer, and can fail with M3_ERR_CUDA.  A
+ *     caller that reserves all free device memory up front makes that
+ *     first call before reserving, and before any stream capture.
  *   - A request that needs more scratch than the buffer holds returns
- *     M3_ERR_SCRATCH and enqueues nothing.  The need is about 33 KB per SM at
- *     N = 128, P = 64 (the buffer covers up to 240 SMs there).
+ *     M3_ERR_SCRATCH and enqueues nothing (strict on purpose: the buffer's
+ *     size is this entry point's stated maximum; m3_scan_prefill serves
+ *     such requests).  The need is about 33 KB per SM at N = 128, P = 64
+ *     (the buffer covers up to 240 SMs there).
  *   - The buffer is shared by every call on a device: calls that overlap in
  *     time (different streams without ordering between them, or different
  *     host threads) race on it.  Order such calls.

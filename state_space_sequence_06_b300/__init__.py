@@ -20,6 +20,9 @@ M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT, M3_E
 M3_F32, M3_BF16 = 0, 1
 M3_ALGO_AUTO, M3_ALGO_RECURRENT, M3_ALGO_CHUNKED = 0, 1, 2
 M3_PRO_DT_SOFTPLUS, M3_PRO_BC_NORM = 1, 2
+# include/m3scan_testing.h
+M3_TEST_KERNEL_NONE, M3_TEST_KERNEL_CHUNKED, M3_TEST_KERNEL_CHUNKED_BALANCED, M3_TEST_KERNEL_RECURRENT = range(4)
+M3_TEST_FAULT_NONE, M3_TEST_FAULT_SKIP_HANDOVER_RELEASE = 0, 1
 
 SYMBOLS = ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
            "m3_decode_step", "m3_device_status", "m3_status_string", "m3_scan_prefill_backward")
@@ -61,7 +64,12 @@ class m3_backward_args(ctypes.Structure):
         [(n, ctypes.c_void_p) for n in ("x", "B", "C", "dt", "lam", "theta", "A", "D", "h0", "prev_B", "prev_x",
                                         "dy", "dh_final", "dx", "dB", "dC", "ddt", "dlam", "dtheta", "dA", "dD",
                                         "dh0", "dprev_B", "dprev_x")] + \
-        [("ngroups", ctypes.c_int32)]
+        [("ngroups", ctypes.c_int32), ("algo", ctypes.c_int32), ("chunk", ctypes.c_int32),
+         ("prologue", ctypes.c_int32), ("dt_bias", ctypes.c_void_p), ("ddt_bias", ctypes.c_void_p)]
+
+
+class m3_launch_info(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("grid", ctypes.c_int32), ("scratch_bytes", ctypes.c_int64)]
 
 
 _lib = None
@@ -84,8 +92,11 @@ def load_library(path: str = LIB_PATH):
     lib.m3_decode_step.argtypes = [ctypes.POINTER(m3_decode_args), vp, vp]
     lib.m3_scan_prefill_backward.argtypes = [ctypes.POINTER(m3_backward_args), vp]
     lib.m3_device_status.argtypes = [vp]
+    lib.m3_test_set_fault.argtypes = [ctypes.c_int32, ctypes.c_int64]
+    lib.m3_test_last_launch.argtypes = [ctypes.POINTER(m3_launch_info)]
     for f in ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",
-              "m3_scan_prefill_noalloc", "m3_decode_step", "m3_device_status", "m3_scan_prefill_backward"):
+              "m3_scan_prefill_noalloc", "m3_decode_step", "m3_device_status", "m3_scan_prefill_backward",
+              "m3_test_set_fault", "m3_test_last_launch"):
         getattr(lib, f).restype = ctypes.c_int
     lib.m3_status_string.argtypes = [ctypes.c_int]
     lib.m3_status_string.restype = ctypes.c_char_p
@@ -242,13 +253,17 @@ def m3_decode_step(x, B, C, dt, lam, theta, A, D, y, state: State, stream=None, 
 
 
 def m3_scan_prefill_backward(x, B, C, dt, lam, theta, A, D, dy, *, h0=None, prev_B=None, prev_x=None,
-                             dh_final=None, stream=None) -> dict:
+                             dh_final=None, algo: int = M3_ALGO_AUTO, chunk: int = 0, prologue: int = 0,
+                             dt_bias=None, stream=None) -> dict:
     """Gradients of a loss with respect to every prefill input, given dy =
     dL/dy [b][L][H][R][P] f32 (and dh_final = dL/dh_final [b][H][N/2][P][2]).
     Inputs as for m3_scan_prefill (fixed-length batch); h0 [b][H][N/2][P][2]
-    f32, prev_B / prev_x the carry.  Returns f32 CUDA tensors dx, dB, dC,
-    ddt, dlam, dtheta, dA, dD, dh0, dprev_B, dprev_x in the inputs' layouts
-    (allocated here; the kernel is the library's)."""
+    f32, prev_B / prev_x the carry.  ``algo``: AUTO (the chunked kernel
+    where the shape has it), RECURRENT (token-serial) or CHUNKED.  With
+    ``prologue`` flags the inputs are raw and the gradients are with respect
+    to them (``ddt_bias`` too).  Returns f32 CUDA tensors dx, dB, dC, ddt,
+    dlam, dtheta, dA, dD, dh0, dprev_B, dprev_x (and ddt_bias) in the
+    inputs' layouts (allocated here; the kernels are the library's)."""
     b, L, H, R, P = x.shape
     N = B.shape[-1]
     f32 = dict(dtype=torch.float32, device=x.device)
@@ -257,9 +272,12 @@ def m3_scan_prefill_backward(x, B, C, dt, lam, theta, A, D, dy, *, h0=None, prev
                dtheta=torch.empty(dt.shape + (N // 2,), **f32), dA=torch.empty(H, **f32),
                dD=torch.empty(H, **f32), dh0=torch.empty((b, H, N // 2, P, 2), **f32),
                dprev_B=torch.empty((b, H, R, N), **f32), dprev_x=torch.empty((b, H, R, P), **f32))
+    if prologue & M3_PRO_DT_SOFTPLUS:
+        out["ddt_bias"] = torch.empty(H, **f32)
     a = m3_backward_args()
     a.dims = m3_dims(b, H, P, N, R, _dtype_code(x))
     a.seqlen, a.ngroups = L, B.shape[2]
+    a.algo, a.chunk, a.prologue, a.dt_bias = algo, chunk, prologue, _ptr(dt_bias)
     for name, t in (("x", x), ("B", B), ("C", C), ("dt", dt), ("lam", lam), ("theta", theta), ("A", A),
                     ("D", D), ("h0", h0), ("prev_B", prev_B), ("prev_x", prev_x), ("dy", dy),
                     ("dh_final", dh_final)):
@@ -272,3 +290,16 @@ def m3_scan_prefill_backward(x, B, C, dt, lam, theta, A, D, dy, *, h0=None, prev
 
 def m3_device_status(stream=None) -> int:
     return load_library().m3_device_status(_stream(stream))
+
+
+def m3_test_set_fault(fault: int, wait_limit_ns: int = 0):
+    """Test hook: plant a fault (M3_TEST_FAULT_*) in the following prefill
+    launches and set their bounded-wait limit (0: the default)."""
+    _check(load_library().m3_test_set_fault(int(fault), int(wait_limit_ns)), "m3_test_set_fault")
+
+
+def m3_test_last_launch() -> m3_launch_info:
+    """Test hook: the kernel, grid and handover scratch of the last prefill."""
+    out = m3_launch_info()
+    _check(load_library().m3_test_last_launch(ctypes.byref(out)), "m3_test_last_launch")
+    return out

@@ -80,7 +80,14 @@ struct ChunkParams {
   __nv_bfloat16* xB;     // handover carry [slot][R][N]
   __nv_bfloat16* xx;     // handover carry [slot][R][P]
   int* xflag;            // [slot]: 1 once the slot is written (zeroed before the launch)
+  // Test hooks (both 0 in normal use): the bounded-wait limit in ns (0:
+  // kWaitLimitNs), and a planted fault (m3_test_fault):
+  // M3_TEST_FAULT_SKIP_HANDOVER_RELEASE makes the writers of the handover
+  // slots leave their flags unset, so the readers' waits run out.
+  unsigned long long wait_ns;
+  int fault;
 };
+
 
 constexpr int kMaxSeg = 8;  // segments per CTA in a balanced schedule
 constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2;
@@ -183,37 +190,42 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Per-CTA abort record in shared memory: the flag that the first role to
+// give up a wait sets, and this launch's wait limit.
+struct CtaAbort {
+  int flag;
+  int pad;
+  unsigned long long limit_ns;
+};
+
 // Bounded wait.  Gives up (and makes every role of this CTA give up) when
-// the phase has not completed within kWaitLimitNs, or as soon as another
-// role of this CTA has recorded a failure, so a stalled pipeline ends each
-// CTA within a fraction of a second with M3_ERR_TIMEOUT.  abort_flag[0] is
-// this CTA's flag.  Waiting threads read nothing outside their own CTA: a
-// poll of a global word by every waiting warp of every CTA costs memory
-// requests the pipeline needs.
+// the phase has not completed within the launch's limit (200 ms unless a
+// test asks for less), or as soon as another role of this CTA has recorded
+// a failure, so a stalled pipeline ends each CTA within a fraction of a
+// second with M3_ERR_TIMEOUT.  Waiting threads read nothing outside their
+// own CTA: a poll of a global word by every waiting warp of every CTA costs
+// memory requests the pipeline needs.
 //
 // Only the first poll is inlined at each call site; the loop is one shared
 // out-of-line copy.  The kernel's roles run different code at the same time
 // on one SM, and instruction fetch is a shared resource: every copy of code
 // that is executed each chunk costs instruction-cache capacity.
-__device__ __noinline__ bool wait_or_abort_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  const uint64_t t0 = globaltimer_ns();
+__device__ __noinline__ bool wait_or_abort_slow(uint32_t bar, uint32_t parity, volatile CtaAbort* ab) {
+  const uint64_t t0 = globaltimer_ns(), limit = ab->limit_ns;
   for (uint32_t i = 1; i < kMaxPolls; ++i) {
     if (umma::mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
-      if (abort_flag[0]) {
-        abort_flag[0] = 1;
-        return false;
-      }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      if (ab->flag) return false;
+      if (globaltimer_ns() - t0 > limit) break;
     }
   }
-  abort_flag[0] = 1;
+  ab->flag = 1;
   atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
   return false;
 }
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile CtaAbort* ab) {
   if (umma::mbar_try_wait(bar, parity)) return true;
-  return wait_or_abort_slow(bar, parity, abort_flag);
+  return wait_or_abort_slow(bar, parity, ab);
 }
 
 template <int N, int R, int Q, bool RE>
@@ -241,8 +253,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB], bar_phend[XB];
   __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_scfull, bar_scfree, bar_rfree;
+  // mdone[i]: every product MMA thread i issued is complete (its last commit,
+  // waited for before the TMEM is freed, also after an abort)
+  __shared__ __align__(8) uint64_t bar_mdone[2];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int s_abort[1];  // this CTA's abort flag
+  __shared__ CtaAbort s_abort;  // this CTA's abort flag and wait limit
   // per-chunk scalars, one set per X slot (chunk c uses slot c % XB)
   __shared__ float sLam[XB][Q], sELam[XB][Q], sGam[XB][Q], sWp[XB][Q], sDw[XB][Q], sLamEnd[XB];
   __shared__ __align__(16) float sBw[XB][Q];
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   auto seg_head = [&](int si) { return sSegHead[si]; };
   auto seg_ntok = [&](int si) { return (int64_t)(sSeg[si].z - sSeg[si].y); };
   auto seg_last = [&](int c) { return c + 1 == sSegC0[seg_of(c) + 1]; };
-  volatile int* abort_flag = s_abort;
+  volatile CtaAbort* abort_flag = &s_abort;
 
   uint8_t* St = sm + Cfg::OFF_ST;
   uint8_t* Stlo = sm + Cfg::OFF_STLO;
@@ -340,7 +355,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   };
 
   if (tid == 0) {
-    s_abort[0] = 0;
+    s_abort.flag = 0;
+    s_abort.limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_full[s]), 1);
       mbar_init(saddr(&bar_opready[s]), 1);
@@ -358,6 +374,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     mbar_init(saddr(&bar_scfull), 1);
     mbar_init(saddr(&bar_scfree), 1);
     mbar_init(saddr(&bar_rfree), 1);
+    mbar_init(saddr(&bar_mdone[0]), 1);
+    mbar_init(saddr(&bar_mdone[1]), 1);
     mbar_init_fence();
   }
   if (warp == 0) {
@@ -695,11 +713,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             ok = true;
             break;
           }
-          if ((i & 63u) == 0 && (abort_flag[0] || globaltimer_ns() - t0 > kWaitLimitNs)) break;
+          if ((i & 63u) == 0 && (abort_flag->flag || globaltimer_ns() - t0 > abort_flag->limit_ns)) break;
         }
         if (!group_and(2, NSTA, ok)) {
           if (tt == 0) {
-            abort_flag[0] = 1;
+            abort_flag->flag = 1;
             atomicExch(&g_status, (int)M3_ERR_TIMEOUT);
           }
           return false;
@@ -757,7 +775,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // phase after its last chunk c) and carry (that token's B and x), to the
     // caller's state or to a handover slot (then published with a release
     // store of the slot's flag)
-    auto finalize = [&](int si, int c) {
+    auto finalize = [&](int si, int c) -> bool {
       const int4 sg = sSeg[si];
       const int unit = sg.x, head = unit % H;
       const bool to_slot = (sg.w & SEG_DST_SLOT) != 0;
@@ -768,7 +786,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (hd) {  // h = e^{i Phi_end} G' (pairs of rows are (re, im) in adjacent lanes)
         // the prologue of chunk c + XB (the slot's next writer) needs the
         // output of chunk c, which follows: this parity wait cannot fall behind
-        if (!wait_or_abort(saddr(&bar_phend[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) return;
+        // (a group vote: every state thread leaves together, or none does)
+        if (!group_and(2, NSTA, wait_or_abort(saddr(&bar_phend[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)))
+          return false;
         float cs = 1.f, sn = 0.f;
         if (g_row >= 0) sincosf(sPhiEndX[c % XB][g_row >> 1], &sn, &cs);
         const bool re = (g_row & 1) == 0;
@@ -797,8 +817,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (to_slot) {
         __threadfence();
         group_sync(2, NSTA);
-        if (tt == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.xflag + slot), "r"(1) : "memory");
+        if (tt == 0 && p.fault != M3_TEST_FAULT_SKIP_HANDOVER_RELEASE)
+          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.xflag + slot), "r"(1) : "memory");
       }
+      return true;
     };
     // X of chunk c to f16 (slot c % XB) and W X as hi (over x) and lo (over
     // theta, or its own area) parts: after the prologue of chunk c (its
@@ -960,7 +982,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             break;
           }
         }
-        if (alive) finalize(si, n - 1);
+        if (alive) alive = finalize(si, n - 1);
       }
       if (alive) output(nchunks - 1, ybf);
     };
@@ -1023,6 +1045,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         mma_commit(saddr(&bar_yfull[s]));
         mma_commit(saddr(&bar_xfree[c % XB]));
       }
+      // on every exit, normal or aborted: no product still writes TMEM when it is freed
+      mma_commit(saddr(&bar_mdone[0]));
+      mbar_wait(saddr(&bar_mdone[0]), 0, kMaxPolls);
     } else if (lane == 0) {
       // MMA 3 (inter-chunk output) and MMA 4 (chunk-local state) of chunk c.
       // MMA 3 needs only this chunk's C and the R of the previous state step,
@@ -1067,6 +1092,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         mma_commit(saddr(&bar_scfull));
         mma_commit(saddr(&bar_free[s]));
       }
+      mma_commit(saddr(&bar_mdone[1]));
+      mbar_wait(saddr(&bar_mdone[1]), 0, kMaxPolls);
     }
   } else {
     // ======================= TMA warp (one thread issues)
@@ -1245,6 +1272,8 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   p.G = G;
   p.pro = a->prologue;
   p.dt_bias = a->dt_bias;
+  p.wait_ns = test_hooks().wait_ns.load();
+  p.fault = test_hooks().fault.load();
   auto kern = chunked_prefill_kernel<N, R, Q, RE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;
@@ -1288,12 +1317,14 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
                                           Cfg::SMEM, s);
         }
         const cudaError_t ef = fixed ? cudaSuccess : cudaFreeAsync(buf, s);
+        record_launch(M3_TEST_KERNEL_CHUNKED_BALANCED, grid, (long long)bytes);
         return (e == cudaSuccess && ef == cudaSuccess) ? M3_OK : M3_ERR_CUDA;
       }
       cudaGetLastError();  // no pool memory: the one-CTA-per-unit launch below
     }
   }
   kern<<<units, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+  record_launch(M3_TEST_KERNEL_CHUNKED, units, 0);
   return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 

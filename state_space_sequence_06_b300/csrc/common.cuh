@@ -5,7 +5,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "m3scan.h"
+#include "m3scan_testing.h"
 
 namespace m3 {
 
@@ -74,5 +77,25 @@ __device__ __forceinline__ void st_y2(void* y, int64_t i, float v0, float v1, bo
 }
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Host-side test hooks (include/m3scan_testing.h): a planted fault and a
+// shorter wait limit for the next prefill launches, and what the last
+// prefill launched.  Atomics, so that concurrent calls never race on them.
+struct TestHooks {
+  std::atomic<int> fault{0};
+  std::atomic<unsigned long long> wait_ns{0};
+  std::atomic<int> last_kernel{0}, last_grid{0};
+  std::atomic<long long> last_scratch{0};
+};
+inline TestHooks& test_hooks() {
+  static TestHooks h;
+  return h;
+}
+inline void record_launch(int kernel, int grid, long long scratch) {
+  TestHooks& t = test_hooks();
+  t.last_kernel.store(kernel);
+  t.last_grid.store(grid);
+  t.last_scratch.store(scratch);
+}
 
 }  // namespace m3

@@ -15,6 +15,7 @@ struct m3_state {
   float* h;
   void* prev_B;
   void* prev_x;
+  cudaStream_t stream;  // the allocation stream: the buffers are stream-ordered on it
 };
 
 namespace {
@@ -189,24 +190,26 @@ m3_status m3_state_alloc(const m3_dims* dims, m3_state** out, void* stream) {
   m3_state* st = new (std::nothrow) m3_state();
   if (!st) return M3_ERR_ALLOC;
   st->dims = *dims;
-  if (cudaMalloc(&st->h, hb) != cudaSuccess) {
-    delete st;
-    return M3_ERR_ALLOC;
-  }
-  if (cudaMalloc(&st->prev_B, bb) != cudaSuccess || cudaMalloc(&st->prev_x, xb) != cudaSuccess) {
-    cudaFree(st->h);
-    cudaFree(st->prev_B);
-    delete st;
-    return M3_ERR_ALLOC;
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st->stream = s;
+  // stream-ordered buffers: m3_state_free returns them on the same stream
+  // without waiting for the device
+  auto release = [&]() {
+    if (st->h) cudaFreeAsync(st->h, s);
+    if (st->prev_B) cudaFreeAsync(st->prev_B, s);
+    if (st->prev_x) cudaFreeAsync(st->prev_x, s);
+    delete st;
+  };
+  if (cudaMallocAsync(reinterpret_cast<void**>(&st->h), hb, s) != cudaSuccess ||
+      cudaMallocAsync(&st->prev_B, bb, s) != cudaSuccess || cudaMallocAsync(&st->prev_x, xb, s) != cudaSuccess) {
+    cudaGetLastError();
+    release();
+    return M3_ERR_ALLOC;
+  }
   if (cudaMemsetAsync(st->h, 0, hb, s) != cudaSuccess ||
       cudaMemsetAsync(st->prev_B, 0, bb, s) != cudaSuccess ||
       cudaMemsetAsync(st->prev_x, 0, xb, s) != cudaSuccess) {
-    cudaFree(st->h);
-    cudaFree(st->prev_B);
-    cudaFree(st->prev_x);
-    delete st;
+    release();
     return M3_ERR_CUDA;
   }
   *out = st;
@@ -215,11 +218,10 @@ m3_status m3_state_alloc(const m3_dims* dims, m3_state** out, void* stream) {
 
 m3_status m3_state_free(m3_state* st) {
   if (!st) return M3_OK;
-  cudaDeviceSynchronize();
   m3_status rc = M3_OK;
-  if (cudaFree(st->h) != cudaSuccess) rc = M3_ERR_CUDA;
-  if (cudaFree(st->prev_B) != cudaSuccess) rc = M3_ERR_CUDA;
-  if (cudaFree(st->prev_x) != cudaSuccess) rc = M3_ERR_CUDA;
+  if (cudaFreeAsync(st->h, st->stream) != cudaSuccess) rc = M3_ERR_CUDA;
+  if (cudaFreeAsync(st->prev_B, st->stream) != cudaSuccess) rc = M3_ERR_CUDA;
+  if (cudaFreeAsync(st->prev_x, st->stream) != cudaSuccess) rc = M3_ERR_CUDA;
   delete st;
   return rc;
 }
@@ -301,12 +303,16 @@ m3_status prefill_impl(const m3_prefill_args* a, m3_state* st, void* stream, voi
   p.L = a->seqlen;
   p.H = a->dims.nheads; p.P = a->dims.headdim; p.N = a->dims.dstate; p.R = a->dims.rank;
   p.G = a->ngroups > 0 ? a->ngroups : a->dims.nheads;
+  m3::record_launch(M3_TEST_KERNEL_RECURRENT, units, 0);
   return bf16 ? recurrent_launch<__nv_bfloat16>(p, a->dims.rank, units, s)
               : recurrent_launch<float>(p, a->dims.rank, units, s);
 }
 
-// The fixed scratch of m3_scan_prefill_noalloc: module memory, reserved when
-// the library is loaded, never allocated by a call.
+// The fixed scratch of m3_scan_prefill_noalloc: module memory of the
+// library.  CUDA creates it on a device when it loads the library's device
+// code there -- under the default lazy module loading, at the first use of
+// the module on that device (the address lookup of the entry point's first
+// call does it); no call allocates it.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[M3_NOALLOC_SCRATCH_BYTES];
 
 }  // namespace
@@ -318,16 +324,35 @@ m3_status m3_scan_prefill(const m3_prefill_args* a, m3_state* st, void* stream) 
 }
 
 m3_status m3_scan_prefill_noalloc(const m3_prefill_args* a, m3_state* st, void* stream) {
-  // the scratch's address on the current device, looked up once per device
-  static void* addr[64] = {};
+  // The scratch's address on the current device, looked up once per device
+  // (atomics: calls from several host threads see either null or the one
+  // address).  The cache assumes that the device's primary context lives as
+  // long as the library: after a device reset the address is stale.
+  static std::atomic<void*> addr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return M3_ERR_CUDA;
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return M3_ERR_CUDA;
-    addr[dev] = p;
+  void* base = addr[dev].load(std::memory_order_acquire);
+  if (!base) {
+    if (cudaGetSymbolAddress(&base, g_noalloc_scratch) != cudaSuccess || !base) return M3_ERR_CUDA;
+    addr[dev].store(base, std::memory_order_release);
   }
-  return prefill_impl(a, st, stream, addr[dev], M3_NOALLOC_SCRATCH_BYTES);
+  return prefill_impl(a, st, stream, base, M3_NOALLOC_SCRATCH_BYTES);
+}
+
+m3_status m3_test_set_fault(int32_t fault, int64_t wait_limit_ns) {
+  if (fault != M3_TEST_FAULT_NONE && fault != M3_TEST_FAULT_SKIP_HANDOVER_RELEASE) return M3_ERR_INVALID_ARG;
+  if (wait_limit_ns < 0) return M3_ERR_INVALID_ARG;
+  m3::test_hooks().fault.store(fault);
+  m3::test_hooks().wait_ns.store((unsigned long long)wait_limit_ns);
+  return M3_OK;
+}
+
+m3_status m3_test_last_launch(m3_launch_info* out) {
+  if (!out) return M3_ERR_INVALID_ARG;
+  out->kernel = m3::test_hooks().last_kernel.load();
+  out->grid = m3::test_hooks().last_grid.load();
+  out->scratch_bytes = m3::test_hooks().last_scratch.load();
+  return M3_OK;
 }
 
 m3_status m3_device_status(void* stream) {

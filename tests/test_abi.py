@@ -57,12 +57,17 @@ def test_host_argument_checks_without_gpu():
     assert lib.m3_scan_prefill(ctypes.byref(a), None, None) == m3.M3_ERR_INVALID_ARG
     assert lib.m3_state_view(None, None) == m3.M3_ERR_INVALID_ARG
     assert lib.m3_state_free(None) == m3.M3_OK
+    # test hooks: unknown faults and negative limits are refused, NULL output too
+    assert lib.m3_test_set_fault(7, 0) == m3.M3_ERR_INVALID_ARG
+    assert lib.m3_test_set_fault(0, -1) == m3.M3_ERR_INVALID_ARG
+    assert lib.m3_test_set_fault(0, 0) == m3.M3_OK
+    assert lib.m3_test_last_launch(None) == m3.M3_ERR_INVALID_ARG
 
 
 def _c_layout(tmp_path, structs):
     """sizeof and offsetof of each field, from the C compiler on the header."""
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "m3scan.h"', '#include "m3scan_backward.h"',
-             "int main(void) {"]
+             '#include "m3scan_testing.h"', "int main(void) {"]
     for st, fields in structs.items():
         lines.append(f'  printf("{st} %zu\\n", sizeof({st}));')
         for f in fields:
@@ -83,7 +88,7 @@ def test_binding_structs_match_the_header_layout(tmp_path):
     size and field offsets (a mismatch would hand the library garbage)."""
     structs = {"m3_dims": m3.m3_dims, "m3_state_ptrs": m3.m3_state_ptrs,
                "m3_prefill_args": m3.m3_prefill_args, "m3_decode_args": m3.m3_decode_args,
-               "m3_backward_args": m3.m3_backward_args}
+               "m3_backward_args": m3.m3_backward_args, "m3_launch_info": m3.m3_launch_info}
     layout = _c_layout(tmp_path, {name: [f for f, _ in cls._fields_] for name, cls in structs.items()})
     for name, cls in structs.items():
         assert layout[name] == ctypes.sizeof(cls), name

@@ -41,3 +41,24 @@ def test_decode_step_bytes():
     assert b["state"] == state == 536_870_912
     # inputs x 128 + B 256 + C 256 + theta 128 + dt + lam 4, carry read and written, y f32
     assert b["per_unit_of_work"] == state + units * 772 + units * 384 * 2 + units * 256 == 551_583_744
+
+
+def test_contraction_flops_against_hand_derived_figures():
+    """Tensor-core work of the chunked form: 2QN + 2QP + 4NP per token and
+    head for SISO (Q 64, N 128, P 64: 57,344, i.e. 60.1 GFLOP for the batch
+    8 x 4096 x 32-head pass); 2QR^2 N + 2QR^2 P + 4RNP for MIMO at Q 16, R 4,
+    N 64; and the issued MMAs with their hi/lo operand pairs (three products
+    for a rotated operand, two for S' and for C R)."""
+    w = synth.workloads()
+    f = bench.contraction_flops(w["siso_b8_l4096"])
+    assert f["per_token_head"] == 57344
+    assert f["algorithmic"] == 57344 * 8 * 4096 * 32
+    # per 64-token chunk: MMA 1 3 x 2*64*64*128, MMA 2 2 x 2*64*64*64, MMA 3 2 x 2*64*64*128, MMA 4 3 x 2*128*64*64
+    per_chunk = 3 * 1048576 + 2 * 524288 + 2 * 1048576 + 3 * 1048576
+    assert f["issued"] == per_chunk * 8 * 4096 * 32 // 64
+    m = bench.contraction_flops(w["mimo4_b8_l4096"])
+    assert m["per_token_head"] == 2 * 16 * 16 * 64 + 2 * 16 * 16 * 64 + 4 * 4 * 64 * 64
+    r = bench.contraction_flops(w["mamba2_b8_l4096"])  # real state: B and C exact in f16, one product each
+    per_chunk_re = 1048576 + 2 * 524288 + 1048576 + 2 * 1048576
+    assert r["issued"] == per_chunk_re * 8 * 4096 * 32 // 64
+    assert bench.contraction_flops(w["decode_siso_b256"]) == {}

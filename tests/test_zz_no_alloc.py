@@ -2,7 +2,9 @@
 the call) against m3_scan_prefill: the same outputs, final state and carry,
 bit for bit, over two chained calls in a row, on a batch that has more
 (sequence, head) units than the GPU has SMs (the schedule that uses
-scratch).  Self-contained: it passes alone and after the other tests."""
+scratch, checked through the library's test hook).  The noalloc call maps
+no device memory (the free memory the driver reports does not change).
+Self-contained: it passes alone and after the other tests."""
 import numpy as np
 import pytest
 import torch
@@ -27,12 +29,21 @@ def test_noalloc_matches_prefill_over_two_calls(shape):
     results = []
     for fn in (m3.m3_scan_prefill, m3.m3_scan_prefill_noalloc):
         st = state_for(dims, inp["h0"], inp["prev_B"], inp["prev_x"])
-        ys = []
-        for _ in range(2):  # the second call continues from the first's state and carry
-            y = torch.empty(tuple(inp["x"].shape), dtype=torch.float32, device="cuda")
-            fn(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], y, state=st)
-            ys.append(y.cpu().numpy())
+        ybuf = [torch.empty(tuple(inp["x"].shape), dtype=torch.float32, device="cuda") for _ in range(2)]
         torch.cuda.synchronize()
+        ys = []
+        for i in range(2):  # the second call continues from the first's state and carry
+            free0 = torch.cuda.mem_get_info()[0]
+            fn(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"], ybuf[i], state=st)
+            info = m3.m3_test_last_launch()
+            torch.cuda.synchronize()
+            # the shape really takes the schedule that uses scratch
+            assert info.kernel == m3.M3_TEST_KERNEL_CHUNKED_BALANCED and info.scratch_bytes > 0
+            if fn is m3.m3_scan_prefill_noalloc and i == 1:
+                # no device memory was mapped by the call (the first call on a
+                # device may load the library's module, so the second is checked)
+                assert torch.cuda.mem_get_info()[0] == free0
+            ys.append(ybuf[i].cpu().numpy())
         assert m3.m3_device_status() == m3.M3_OK
         h, pB, px = st.views()
         results.append((ys, to_np(h), to_np(pB), to_np(px)))
