@@ -613,16 +613,43 @@ def contract_line(head, cpu, others, args, world):
     }
 
 
+def backward_flops(wl) -> int:
+    """Contraction FLOPs of one chunked backward pass: per chunk of MR = QR
+    rows, the chunk sums Z = Bt^T (f x) and U = Ct^T (e^Lam dy) (2 N MR P
+    each), and the gradient contractions: S and dM (2 MR^2 N, 2 MR^2 P), the
+    inter output Ct Gs (2 MR P N), dX = M^T dY + Bt dG (2 MR^2 P + 2 MR N P),
+    dCt = dS Bt + dY Gs^T and dBt = dS^T Ct + X dG^T (2 (2 MR^2 N + 2 MR N P))."""
+    Q, R, N, P = 64 // wl.rank, wl.rank, wl.dstate, wl.headdim
+    MR = Q * R
+    per_chunk = (2 * (2 * N * MR * P) + 2 * MR * MR * N + 2 * MR * MR * P + 2 * MR * P * N
+                 + 2 * MR * MR * P + 2 * MR * N * P + 2 * (2 * MR * MR * N + 2 * MR * N * P))
+    nch = -(-wl.seqlen // Q)
+    return per_chunk * nch * wl.batch * wl.nheads
+
+
+def fp32_peak_tflops():
+    """FP32 FMA peak of a B300 from its unit counts and clock: 148 SMs x 128
+    FP32 lanes x 2 FLOP per FMA x the maximum SM clock (2032 MHz)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2032.0
+    return 148 * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
-    """Time m3_scan_prefill_backward (the token-serial reference kernel) on
-    a prefill workload with a seeded dL/dy and dL/dh_final; one pass = every
-    gradient of the batch.  Algorithmic bytes: the forward inputs and dL/dy
-    read once, every gradient written once (the kernel's own history
-    scratch is not counted).  Unit 0's dx and ddt are checked against the
+    """Time m3_scan_prefill_backward on a prefill workload with a seeded
+    dL/dy and dL/dh_final; one pass = every gradient of the batch (the
+    chunked kernels where the shape has them: --algo auto or chunked; the
+    token-serial kernel: --algo recurrent).  Roofline: the contraction
+    FLOPs of the chunked form against the FP32 FMA peak (the kernels are
+    f32 SIMT: bound "alu").  Unit 0's gradients are checked against the
     oracle's adjoint."""
     import oracle
 
     H, P, N, R, L, b = wl.nheads, wl.headdim, wl.dstate, wl.rank, wl.seqlen, wl.batch
+    algo = {"auto": m3.M3_ALGO_AUTO, "recurrent": m3.M3_ALGO_RECURRENT, "chunked": m3.M3_ALGO_CHUNKED}[args.algo]
     inp = synth.prefill_inputs(wl)
     rng = np.random.default_rng(0)
     dy = rng.normal(size=(b, L, H, R, P)).astype(np.float32)
@@ -634,22 +661,23 @@ def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
     def once():
         return m3.m3_scan_prefill_backward(t["x"], t["B"], t["C"], t["dt"], t["lam"], t["theta"], t["A"], t["D"],
                                            dy_d, h0=t["h0"], prev_B=t["prev_B"], prev_x=t["prev_x"],
-                                           dh_final=dhf_d)
+                                           dh_final=dhf_d, algo=algo)
 
     for _ in range(args.warmup):
         out = once()
     torch.cuda.synchronize()
+    steps = args.steps if algo != m3.M3_ALGO_RECURRENT else min(args.steps, 3)
     with ClockSampler(local) as clk:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             out = once()
         e1.record(stream)
         torch.cuda.synchronize()
     total_ms = max_over_ranks(torch, dist, world, e0.elapsed_time(e1), "cuda")
     status = m3.m3_device_status()
     # parity of unit 0 (sequence 0, head 0) against the adjoint oracle
-    w = lambda k: oracle._widen(inp[k], wl.dtype)
+    w = lambda k: oracle._widen(inp[k], wl.dtype)  # noqa: E731
     g = 0  # head 0 reads group 0
     _, _, ref = oracle.unit_backward(w("x")[0, :, 0], w("B")[0, :, g], w("C")[0, :, g], w("dt")[0, :, 0],
                                      w("lam")[0, :, 0], w("theta")[0, :, 0], float(inp["A"][0]),
@@ -657,7 +685,7 @@ def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
                                      w("prev_B")[0, 0], w("prev_x")[0, 0], dy[0, :, 0].astype(np.float64),
                                      dhf[0, 0, ..., 0] + 1j * dhf[0, 0, ..., 1])
     err = {}
-    for gk, rk in (("dx", "x"), ("ddt", "dt")):
+    for gk, rk in (("dx", "x"), ("dB", "B"), ("dC", "C"), ("ddt", "dt"), ("dlam", "lam"), ("dtheta", "theta")):
         got = out[gk][0, :, 0].double().cpu().numpy()
         err[gk] = float(np.max(np.abs(got - ref[rk])) / max(np.sqrt(np.mean(ref[rk] ** 2)), 1e-30))
     isz = 2 if wl.dtype == "bf16" else 4
@@ -665,21 +693,27 @@ def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
     in_bytes = th * (R * P + 2 * R * N + 2 + N // 2) * isz + th * R * P * 4
     out_bytes = th * (R * P + 2 * R * N + 2 + N // 2) * 4
     byt = in_bytes + out_bytes
-    per_ms = total_ms / args.steps
+    per_ms = total_ms / steps
     hbm_peak, _, peak_src = peaks()
-    achieved = byt / (per_ms / 1e3) / 1e9
+    flops = backward_flops(wl)
+    alu_peak = fp32_peak_tflops()
+    achieved = flops / (per_ms / 1e3) / 1e12
     if rank == 0:
+        kernel = "token-serial" if algo == m3.M3_ALGO_RECURRENT else "chunked (f32 SIMT)"
         print(json.dumps({
-            "metric": "Mamba-3 scan backward tokens/s (token-serial reference kernel)",
-            "value": b * L * world / (per_ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(config_of(wl), **{"pass": "backward (all gradients, f32)"}),
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
-                         "algorithmic_bytes_per_launch": byt},
-            "gpu_launches": args.steps, "device_status": status, "clocks": clk.summary(),
-            "parity": {"unit": 0, "max_err_over_rms": err}}), flush=True)
+            "metric": "Mamba-3 scan backward tokens/s", "value": b * L * world / (per_ms / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": per_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(config_of(wl), **{"pass": "backward (all gradients, f32)", "kernel": kernel}),
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                         "frac": achieved / alu_peak, "traffic": None,
+                         "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x max SM clock",
+                         "flops_per_launch": flops, "kernel_ms_per_launch": per_ms,
+                         "hbm": {"algorithmic_bytes_per_launch": byt, "achieved_gbs": byt / (per_ms / 1e3) / 1e9,
+                                 "peak": hbm_peak, "frac": byt / (per_ms / 1e3) / 1e9 / hbm_peak,
+                                 "peak_source": peak_src}},
+            "gpu_launches": steps * (1 if algo == m3.M3_ALGO_RECURRENT else 5), "device_status": status,
+            "clocks": clk.summary(), "parity": {"unit": 0, "max_err_over_rms": err}}), flush=True)
 
 
 def sampled_parity(wl, m3, t, y, st, cu, algo):

@@ -181,9 +181,13 @@ def workloads() -> dict:
         # the same SISO prefill from raw inputs: dt before softplus, B and C before the RMS norm
         "siso_prologue_b8_l4096": Workload("siso_prologue_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16",
                                            chunk=64, prologue=True),
-        # the backward pass of a prefill (token-serial reference kernel), batch 2, L 1024
+        # the backward pass of a prefill: batch 2, L 1024, and the SISO layer shape of the prefill line
         "backward_siso_b2_l1024": Workload("backward_siso_b2_l1024", "prefill", 2, 1024, 32, 64, 128, 1, "bf16",
                                            h0_std=0.1, carry=True, backward=True),
+        "backward_siso_b8_l4096": Workload("backward_siso_b8_l4096", "prefill", 8, 4096, 32, 64, 128, 1, "bf16",
+                                           h0_std=0.1, carry=True, backward=True),
+        "backward_mimo4_b8_l4096": Workload("backward_mimo4_b8_l4096", "prefill", 8, 4096, 32, 64, 64, 4, "bf16",
+                                            chunk=16, h0_std=0.1, carry=True, backward=True),
         "varlen_16": Workload(
             "varlen_16", "varlen", 1, 0, 32, 64, 128, 1, "bf16", chunk=64, dt_shift=-3.0,
             nseq=16, len_lo=256, len_hi=8192,

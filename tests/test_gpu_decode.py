@@ -114,3 +114,34 @@ def test_decode_full_size_sampled(name):
     units = sorted(set([0, wl.batch * wl.nheads - 1] + list(rng.choice(wl.batch * wl.nheads, 10, replace=False))))
     gpu, ref = run_decode(wl, wl.seqlen, units=units, window=128)
     check(gpu, ref, wl.dtype, name)
+
+
+@pytest.mark.parametrize("name", ["decode_siso_b256", "decode_mimo4_b256"])
+def test_decode_full_size_every_unit(name):
+    """Every unit of the full workload (batch 256, 32 heads: 8192 units) for
+    256 steps, in the benchmark's launch configuration: every output of
+    every step and the whole final state against the oracle, the carry bit
+    for bit.  (The sampled test above walks all 1024 steps.)"""
+    wl = synth.workloads()[name]
+    steps = 256
+    b, H, P, N, R = wl.batch, wl.nheads, wl.headdim, wl.dstate, wl.rank
+    d = synth.decode_inputs(wl, steps=steps)
+    st = state_for((b, H, P, N, R, m3.M3_BF16), d["h0"], d["prev_B"], d["prev_x"])
+    t = {k: dev(d[k]) for k in ("x", "B", "C", "dt", "lam", "theta", "A", "D")}
+    ys = torch.empty((steps, b, H, R, P), dtype=torch.float32, device="cuda")
+    for i in range(steps):
+        m3.m3_decode_step(t["x"][i], t["B"][i], t["C"][i], t["dt"][i], t["lam"][i], t["theta"][i], t["A"], t["D"],
+                          ys[i], st)
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    h, pB, px = st.views()
+    gh, gpB, gpx = to_np(h), to_np(pB), to_np(px)
+    gy = ys.cpu().numpy().astype(np.float64)
+    st.free()
+    yo, ho, pBo, pxo = oracle.decode(d, batch=b, H=H, P=P, N=N, R=R, dtype=wl.dtype, steps=steps)
+    tol = TOL[wl.dtype]
+    ey = np.max(np.abs(gy - yo)) / np.sqrt(np.mean(yo ** 2))
+    eh = np.max(np.abs(gh.reshape(ho.shape) - ho)) / np.sqrt(np.mean(ho ** 2))
+    assert ey <= tol, f"{name} y over every unit: {ey:.3e}"
+    assert eh <= tol, f"{name} h_final over every unit: {eh:.3e}"
+    assert np.array_equal(gpB.reshape(pBo.shape), pBo) and np.array_equal(gpx.reshape(pxo.shape), pxo)
