@@ -23,7 +23,9 @@ typedef enum m3_test_kernel {
   M3_TEST_KERNEL_NONE = 0,
   M3_TEST_KERNEL_CHUNKED = 1,          /* tensor-core kernel, one CTA per (sequence, head) unit */
   M3_TEST_KERNEL_CHUNKED_BALANCED = 2, /* tensor-core kernel, balanced schedule (handover scratch) */
-  M3_TEST_KERNEL_RECURRENT = 3         /* token-serial kernel */
+  M3_TEST_KERNEL_RECURRENT = 3,        /* token-serial kernel */
+  M3_TEST_KERNEL_CHUNKED_SPLIT = 4     /* tensor-core kernel, split schedule (few units: segments of each unit
+                                          in parallel, a state-only pass first) */
 } m3_test_kernel;
 
 /* Planted faults (m3_test_set_fault). */
@@ -40,8 +42,8 @@ typedef enum m3_test_fault {
 /* What the last prefill launched (from any host thread). */
 typedef struct m3_launch_info {
   int32_t kernel;        /* m3_test_kernel */
-  int32_t grid;          /* CTAs launched */
-  int64_t scratch_bytes; /* handover scratch the launch used (balanced schedule), else 0 */
+  int32_t grid;          /* CTAs launched (per pass) */
+  int64_t scratch_bytes; /* handover scratch the launch used (balanced or split schedule), else 0 */
 } m3_launch_info;
 
 /*

@@ -21,7 +21,8 @@ M3_F32, M3_BF16 = 0, 1
 M3_ALGO_AUTO, M3_ALGO_RECURRENT, M3_ALGO_CHUNKED = 0, 1, 2
 M3_PRO_DT_SOFTPLUS, M3_PRO_BC_NORM = 1, 2
 # include/m3scan_testing.h
-M3_TEST_KERNEL_NONE, M3_TEST_KERNEL_CHUNKED, M3_TEST_KERNEL_CHUNKED_BALANCED, M3_TEST_KERNEL_RECURRENT = range(4)
+(M3_TEST_KERNEL_NONE, M3_TEST_KERNEL_CHUNKED, M3_TEST_KERNEL_CHUNKED_BALANCED, M3_TEST_KERNEL_RECURRENT,
+ M3_TEST_KERNEL_CHUNKED_SPLIT) = range(5)
 M3_TEST_FAULT_NONE, M3_TEST_FAULT_SKIP_HANDOVER_RELEASE = 0, 1
 
 SYMBOLS = ("m3_state_alloc", "m3_state_free", "m3_state_view", "m3_scan_prefill",

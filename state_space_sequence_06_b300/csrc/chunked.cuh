@@ -86,11 +86,24 @@ struct ChunkParams {
   // slots leave their flags unset, so the readers' waits run out.
   unsigned long long wait_ns;
   int fault;
+  // Split schedule (split_S > 0): unit u is cut into split_S segments of
+  // split_len chunks, CTA u * split_S + s running segment s.  The
+  // state-only pass (the kernel's SO variant) runs every segment from the
+  // zero state with the carry of its previous token (handover slot
+  // blockIdx.x), writes the segment's own final state to seg_h and its total
+  // decay and rotation e^{Lam + i Phi} per pair to seg_alpha; the full pass
+  // then runs every segment from its exact initial state (slot blockIdx.x,
+  // combined from those on the device), and only the last segment of a
+  // unit writes the caller's state.
+  int split_S;
+  int split_len;
+  float* seg_h;         // [unit * split_S + s][K2][P][2]
+  float2* seg_alpha;    // [unit * split_S + s][K2]
 };
 
 
 constexpr int kMaxSeg = 8;  // segments per CTA in a balanced schedule
-constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2;
+constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2, SEG_NO_FINAL = 4;
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -228,7 +241,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return wait_or_abort_slow(bar, parity, ab);
 }
 
-template <int N, int R, int Q, bool RE>
+// SO: the state-only pass of the split schedule: no C, no scores, no
+// outputs; MMA 4 and the state chain only, each segment's final state and
+// total decay and rotation to seg_h / seg_alpha.
+template <int N, int R, int Q, bool RE, bool SO = false>
 __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                            const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_th,
@@ -310,6 +326,17 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (head_seg.w >= 0) sSeg[ns++] = head_seg;
       for (int i = 0; i < nmid; ++i) sSeg[ns++] = mid[i];
       if (tail_seg.w >= 0) sSeg[ns++] = tail_seg;
+    } else if (p.split_S) {
+      // segment s of unit u; its handover slot is blockIdx.x
+      const int u = blockIdx.x / p.split_S, sgi = blockIdx.x % p.split_S;
+      const int64_t tb = (int64_t)sgi * p.split_len * Q, te0 = tb + (int64_t)p.split_len * Q;
+      const int64_t te = te0 < p.L ? te0 : p.L;
+      int fl = (int)blockIdx.x << 8;
+      if (SO)
+        fl |= SEG_SRC_SLOT | SEG_DST_SLOT;  // from the zero state and the previous token's carry
+      else
+        fl |= (sgi > 0 ? SEG_SRC_SLOT : 0) | (sgi + 1 < p.split_S ? SEG_NO_FINAL : 0);
+      if (tb < te) sSeg[ns++] = make_int4(u, (int)tb, (int)te, fl);
     } else {
       const int u = blockIdx.x, sq = u / H;
       const int n = p.cu_seqlens ? p.cu_seqlens[sq + 1] - p.cu_seqlens[sq] : (int)p.L;
@@ -360,12 +387,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_full[s]), 1);
       mbar_init(saddr(&bar_opready[s]), 1);
-      mbar_init(saddr(&bar_free[s]), 2);   // MMA 1 and MMAs 4/3 completions
+      mbar_init(saddr(&bar_free[s]), SO ? 1 : 2);   // MMA 1 and MMAs 4/3 completions (SO: MMA 4)
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
     }
     for (int x = 0; x < XB; ++x) {
-      mbar_init(saddr(&bar_xfree[x]), 2);   // MMA 2 completion and the output epilogue
+      // MMA 2 completion and the output epilogue (SO: the state warps, once
+      // the slot's scalars are no longer read)
+      mbar_init(saddr(&bar_xfree[x]), SO ? 1 : 2);
       mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X
       mbar_init(saddr(&bar_phend[x]), K2);  // the phase after the slot's chunk, one arrival per pair
     }
@@ -440,7 +469,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         //      as it landed; TPR adjacent threads per row, 16-byte chunks
         constexpr int TPR = NPRO / (2 * MR), CPT = N / 8 / TPR;
         const int row = pt / TPR, part = pt % TPR;
-        const bool isC = row >= MR;
+        const bool isC = row >= MR;  // (SO: no C tile; those threads' sums are unused)
         const int rr = isC ? row - MR : row;
         const uint8_t* base = stg + (isC ? Cfg::OFF_C : Cfg::OFF_B);
         const uint32_t blk_bytes = isC ? (uint32_t)(MR * 128) : (uint32_t)Cfg::BB;
@@ -527,9 +556,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             const uint32_t rc = sw128_offset(i * R + r, col);
             const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
             const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
-            const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
             *reinterpret_cast<uint32_t*>(Bt + ob) = pack_half2(b.x, b.y);
-            *reinterpret_cast<uint32_t*>(Ct + o) = pack_half2(cc.x, cc.y);
+            if (!SO) {
+              const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
+              *reinterpret_cast<uint32_t*>(Ct + o) = pack_half2(cc.x, cc.y);
+            }
           }
         }
       } else {
@@ -568,21 +599,26 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             const uint32_t rc = sw128_offset(i * R + r, col);
             const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
             float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
-            float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
             if constexpr (NORM) {
-              const float fb = sBScl[i * R + r], fc = sCScl[i * R + r];
+              const float fb = sBScl[i * R + r];
               b.x *= fb;
               b.y *= fb;
-              cc.x *= fc;
-              cc.y *= fc;
             }
             uint32_t hi, lo;
             split_half2(cs[ii] * b.x - sn[ii] * b.y, sn[ii] * b.x + cs[ii] * b.y, hi, lo);
             *reinterpret_cast<uint32_t*>(Bt + ob) = hi;
             *reinterpret_cast<uint32_t*>(Blo + ob) = lo;
-            split_half2(cs[ii] * cc.x - sn[ii] * cc.y, sn[ii] * cc.x + cs[ii] * cc.y, hi, lo);
-            *reinterpret_cast<uint32_t*>(Ct + o) = hi;
-            *reinterpret_cast<uint32_t*>(Clo + o) = lo;
+            if (!SO) {  // (the state-only pass has no C)
+              float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
+              if constexpr (NORM) {
+                const float fc = sCScl[i * R + r];
+                cc.x *= fc;
+                cc.y *= fc;
+              }
+              split_half2(cs[ii] * cc.x - sn[ii] * cc.y, sn[ii] * cc.x + cs[ii] * cc.y, hi, lo);
+              *reinterpret_cast<uint32_t*>(Ct + o) = hi;
+              *reinterpret_cast<uint32_t*>(Clo + o) = lo;
+            }
           }
         }
         if (g == 0) {  // the running phase after this chunk, reduced to [-pi, pi)
@@ -680,7 +716,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       bool alive = prologue(0, normtag);
       for (int c = 0; c < nchunks && alive; ++c) {
         if (c + 1 < nchunks && !prologue(c + 1, normtag)) break;
-        alive = scores(c);
+        if (!SO) alive = scores(c);
       }
     };
     if (!RE && (p.pro & M3_PRO_BC_NORM))
@@ -698,8 +734,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // (zero without one) or from a handover slot, whose writer publishes it
     // with a release store of its flag; also R = f16(G') for the first MMA 3
     // of the segment.
+    // product of the segment's chunk decays (the state-only pass reports it)
+    float seg_decay = 1.f;
     auto init_seg = [&](int si) -> bool {
       const int4 sg = sSeg[si];
+      seg_decay = 1.f;
       const int unit = sg.x, head = unit % H;
       const bool from_slot = (sg.w & SEG_SRC_SLOT) != 0;
       const int slot = sg.w >> 8;
@@ -756,7 +795,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           }
         }
         tmem_st16(tmem + lane_base + Cfg::COL_G + cb, v);
-        if (g_row >= 0) {  // R = f16(G') for MMA 3 of the segment's first chunk
+        if (!SO && g_row >= 0) {  // R = f16(G') for MMA 3 of the segment's first chunk
 #pragma unroll
           for (int pc = 0; pc < 16; pc += 8)
             *reinterpret_cast<uint4*>(Rt + sw128_offset(g_row, cb + pc)) =
@@ -768,21 +807,27 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       fence_async_smem();
       tc_fence_before();
       group_sync(2, NSTA);
-      if (tt == 0) mbar_arrive(saddr(&bar_stready));
+      if (!SO && tt == 0) mbar_arrive(saddr(&bar_stready));
       return true;
     };
     // final state of segment si (h of its last token, rotated back by the
     // phase after its last chunk c) and carry (that token's B and x), to the
     // caller's state or to a handover slot (then published with a release
     // store of the slot's flag)
+    // (the state-only pass: the segment's own final state to seg_h and its
+    // decay and rotation e^{Lam + i Phi} to seg_alpha, then the release of
+    // the last chunk's scalar slot; a segment that a later one continues in
+    // a split schedule writes nothing)
     auto finalize = [&](int si, int c) -> bool {
       const int4 sg = sSeg[si];
       const int unit = sg.x, head = unit % H;
-      const bool to_slot = (sg.w & SEG_DST_SLOT) != 0;
+      if (!SO && (sg.w & SEG_NO_FINAL)) return true;
+      const bool to_slot = !SO && (sg.w & SEG_DST_SLOT) != 0;
       const int slot = sg.w >> 8;
-      float* hd = to_slot ? p.xh + (int64_t)slot * K2 * P * 2 : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr);
-      __nv_bfloat16* cB = to_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
-      __nv_bfloat16* cx = to_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
+      float* hd = SO ? p.seg_h + (int64_t)slot * K2 * P * 2
+                     : (to_slot ? p.xh + (int64_t)slot * K2 * P * 2 : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr));
+      __nv_bfloat16* cB = SO ? nullptr : to_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
+      __nv_bfloat16* cx = SO ? nullptr : to_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
       if (hd) {  // h = e^{i Phi_end} G' (pairs of rows are (re, im) in adjacent lanes)
         // the prologue of chunk c + XB (the slot's next writer) needs the
         // output of chunk c, which follows: this parity wait cannot fall behind
@@ -792,6 +837,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         float cs = 1.f, sn = 0.f;
         if (g_row >= 0) sincosf(sPhiEndX[c % XB][g_row >> 1], &sn, &cs);
         const bool re = (g_row & 1) == 0;
+        if (SO && g_row >= 0 && re)
+          p.seg_alpha[(int64_t)slot * K2 + (g_row >> 1)] = make_float2(seg_decay * cs, seg_decay * sn);
         for (int cb = 0; cb < P; cb += 16) {
           float v[16];
           tmem_ld16(tmem + lane_base + Cfg::COL_G + cb, v);
@@ -820,6 +867,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         if (tt == 0 && p.fault != M3_TEST_FAULT_SKIP_HANDOVER_RELEASE)
           asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.xflag + slot), "r"(1) : "memory");
       }
+      if (SO) {  // the last chunk's scalars (its phase) are read: release the slot
+        group_sync(2, NSTA);
+        if (tt == 0) mbar_arrive(saddr(&bar_xfree[c % XB]));
+      }
       return true;
     };
     // X of chunk c to f16 (slot c % XB) and W X as hi (over x) and lo (over
@@ -829,7 +880,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const int s = c & 1, xs = c % XB;
       uint8_t* stg = stage(s);
       bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
-      if (got && c >= XB) got = wait_xfree(c - XB);
+      if (!SO && got && c >= XB) got = wait_xfree(c - XB);  // (SO: no X slot)
       if (!group_and(2, NSTA, got)) return false;
       {
         uint8_t* Xs = stg + Cfg::OFF_X;
@@ -849,7 +900,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             hx[q] = pack_half2(f.x, f.y);
             split_half2(w * f.x, w * f.y, hw[q], lw[q]);
           }
-          *reinterpret_cast<uint4*>(Xb + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
+          if (!SO) *reinterpret_cast<uint4*>(Xb + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
           *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
@@ -867,10 +918,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const int xs = c % XB;
       const bool pub = !seg_last(c);
       bool got = wait_or_abort(saddr(&bar_scfull), (uint32_t)(c & 1), abort_flag);
-      if (got) got = wait_or_abort(saddr(&bar_rfree), (uint32_t)(c & 1), abort_flag);
+      if (!SO && got) got = wait_or_abort(saddr(&bar_rfree), (uint32_t)(c & 1), abort_flag);
       if (!group_and(2, NSTA, got)) return false;
       tc_fence_after();
       const float elam_end = __expf(sLamEnd[xs]);
+      seg_decay *= elam_end;
 #pragma unroll 1
       for (int hc = 0; hc < P; hc += 16) {
         float g[16], sc[16];
@@ -880,7 +932,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) g[i] = fmaf(elam_end, g[i], sc[i]);
         tmem_st16(tmem + lane_base + Cfg::COL_G + hc, g);
-        if (pub && g_row >= 0) {
+        if (!SO && pub && g_row >= 0) {
 #pragma unroll
           for (int pc = 0; pc < 16; pc += 8)
             *reinterpret_cast<uint4*>(Rt + sw128_offset(g_row, hc + pc)) =
@@ -893,8 +945,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       tc_fence_before();
       group_sync(2, NSTA);
       if (tt == 0) {
-        if (pub) mbar_arrive(saddr(&bar_stready));
+        if (!SO && pub) mbar_arrive(saddr(&bar_stready));
         mbar_arrive(saddr(&bar_scfree));
+        // the state-only pass releases the chunk's scalar slot here (the
+        // segment's last chunk: after finalize has read its phase)
+        if (SO && pub) mbar_arrive(saddr(&bar_xfree[xs]));
       }
       return true;
     };
@@ -977,14 +1032,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         if (!init_seg(si)) break;
         const int end = sSegC0[si + 1];
         for (; n < end; ++n) {
-          if (!xconv(n) || (n >= 1 && !output(n - 1, ybf)) || !state(n)) {
+          if (!xconv(n) || (!SO && n >= 1 && !output(n - 1, ybf)) || !state(n)) {
             alive = false;
             break;
           }
         }
         if (alive) alive = finalize(si, n - 1);
       }
-      if (alive) output(nchunks - 1, ybf);
+      if (!SO && alive) output(nchunks - 1, ybf);
     };
     if (p.ybf)
       run(BoolTag<true>{});
@@ -1000,7 +1055,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     auto mnmaj = [](uint32_t base, int ks, uint32_t lbo) {
       return smem_desc(base + ks * 2048, lbo, 1024, kSwizzle128B);
     };
-    if (lane == 0 && warp == Cfg::W_MMA) {
+    if (lane == 0 && warp == Cfg::W_MMA && !SO) {  // (the state-only pass has no intra-chunk products)
       // intra-chunk products, MMA 1 one chunk ahead of MMA 2
       auto mma1 = [&](int c) -> bool {
         const int s = c & 1;
@@ -1048,7 +1103,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       // on every exit, normal or aborted: no product still writes TMEM when it is freed
       mma_commit(saddr(&bar_mdone[0]));
       mbar_wait(saddr(&bar_mdone[0]), 0, kMaxPolls);
-    } else if (lane == 0) {
+    } else if (lane == 0 && warp == Cfg::W_MMA2) {
       // MMA 3 (inter-chunk output) and MMA 4 (chunk-local state) of chunk c.
       // MMA 3 needs only this chunk's C and the R of the previous state step,
       // so it goes first; the stage is released when MMA 4 is done.
@@ -1061,20 +1116,22 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         // C of the stage rotated (prologue); R of the state at the start of chunk c
         // written; Yi[s] free (output of chunk c - 2 done)
         if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
-        if (!wait_or_abort(saddr(&bar_stready), (uint32_t)(c & 1), abort_flag)) break;
-        if (c >= 2 && !wait_xfree(c - 2)) break;
-        tc_fence_after();
-        {  // Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
-          constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
+        if (!SO) {
+          if (!wait_or_abort(saddr(&bar_stready), (uint32_t)(c & 1), abort_flag)) break;
+          if (c >= 2 && !wait_xfree(c - 2)) break;
+          tc_fence_after();
+          {  // Yi[s] = C R = Chi R + Clo R   (M = MR, N = P, K = N)
+            constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
 #pragma unroll 1
-          for (int ks = 0; ks < N / 16; ++ks) {
-            mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Ct, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, ks > 0);
-            if (!RE)
-              mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
+            for (int ks = 0; ks < N / 16; ++ks) {
+              mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Ct, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, ks > 0);
+              if (!RE)
+                mma_f16(tmem + Cfg::COL_YI + s * P, kmaj(Clo, ks, MR * 128), mnmaj(saddr(Rt), ks, N * 128), idesc, 1);
+            }
           }
+          mma_commit(saddr(&bar_rfree));
+          mma_commit(saddr(&bar_yfull[s]));
         }
-        mma_commit(saddr(&bar_rfree));
-        mma_commit(saddr(&bar_yfull[s]));
         // W X converted (state warps); S_{c-1} folded into the state
         if (!wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;
         if (c >= 1 && !wait_or_abort(saddr(&bar_scfree), (uint32_t)((c - 1) & 1), abort_flag)) break;
@@ -1106,12 +1163,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         const uint32_t bar = saddr(&bar_full[s]);
         const int si = seg_of(c), head = seg_head(si);
         const int t = (int)(sSegTok0[si] + (int64_t)(c - sSegC0[si]) * Q);
-        mbar_arrive_expect_tx(bar, Cfg::STAGE_TX);
+        mbar_arrive_expect_tx(bar, SO ? Cfg::STAGE_TX - Cfg::CT_BYTES : Cfg::STAGE_TX);  // (SO: no C tile)
         tma_load_4d(saddr(stg + Cfg::OFF_X), &tm_x, bar, 0, 0, head, t);
 #pragma unroll
         for (int kb = 0; kb < N / 64; ++kb) {
           tma_load_4d(saddr(stg + Cfg::OFF_B + kb * Cfg::BB), &tm_B, bar, 64 * kb, 0, head / hpg, t);
-          tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head / hpg, t);
+          if (!SO) tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head / hpg, t);
         }
         if (!RE) tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
         if (s) ++issued1; else ++issued0;
@@ -1126,13 +1183,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
 #pragma unroll
         for (int kb = 0; kb < N / 64; ++kb) {
           tma_prefetch_4d(&tm_B, 64 * kb, 0, head / hpg, t);
-          tma_prefetch_4d(&tm_C, 64 * kb, 0, head / hpg, t);
+          if (!SO) tma_prefetch_4d(&tm_C, 64 * kb, 0, head / hpg, t);
         }
         if (!RE) tma_prefetch_3d(&tm_th, 0, head, t);
       };
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_B);
-      tma_prefetch_desc(&tm_C);
+      if (!SO) tma_prefetch_desc(&tm_C);
       if (!RE) tma_prefetch_desc(&tm_th);
       issue(0);
       if (nchunks > 1) issue(1);
@@ -1236,6 +1293,49 @@ inline cudaMemPool_t handover_pool(int dev) {
   return pools[dev];
 }
 
+// Split schedule, before the state-only pass: handover slot u * S + s gets
+// the zero state and the carry of its segment's previous token (segment 0:
+// the caller's carry, or none), and its flag is set (nothing waits on it).
+template <int N, int R, int Q>
+__global__ void __launch_bounds__(256) split_prep_kernel(const ChunkParams p) {
+  constexpr int K2 = N / 2, P = 64;
+  const int slot = blockIdx.x, u = slot / p.split_S, sgi = slot % p.split_S;
+  const int head = u % p.H, b = u / p.H;
+  float* xh = p.xh + (int64_t)slot * K2 * P * 2;
+  for (int i = threadIdx.x; i < K2 * P * 2; i += blockDim.x) xh[i] = 0.f;
+  const __nv_bfloat16 zero = __float2bfloat16(0.f);
+  __nv_bfloat16* cB = p.xB + (int64_t)slot * R * N;
+  __nv_bfloat16* cx = p.xx + (int64_t)slot * R * P;
+  const int64_t t = (int64_t)b * p.L + (int64_t)sgi * p.split_len * Q - 1;  // the previous token
+  const int64_t browB = (t * p.G + head / (p.H / p.G)) * R * N, browx = (t * p.H + head) * R * P;
+  for (int i = threadIdx.x; i < R * N; i += blockDim.x)
+    cB[i] = sgi > 0 ? p.B[browB + i] : (p.prev_B ? p.prev_B[(int64_t)u * R * N + i] : zero);
+  for (int i = threadIdx.x; i < R * P; i += blockDim.x)
+    cx[i] = sgi > 0 ? p.x[browx + i] : (p.prev_x ? p.prev_x[(int64_t)u * R * P + i] : zero);
+  if (threadIdx.x == 0) p.xflag[slot] = 1;
+}
+
+// Split schedule, between the two passes: the initial state of every
+// segment, h_in(s + 1) = alpha_s * h_in(s) + h_loc(s) with h_in(0) the
+// caller's state (zero without one), per pair and column, into the
+// segment's handover slot.  Exact: the recurrence is affine in the state,
+// and h_loc(s) already holds the segment's carry term.
+template <int N>
+__global__ void __launch_bounds__(256) split_combine_kernel(const ChunkParams p, int units) {
+  constexpr int K2 = N / 2, P = 64, KP = K2 * P;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)units * KP) return;
+  const int u = (int)(i / KP), e = (int)(i % KP), k = e / P;
+  float2 h = p.h ? reinterpret_cast<const float2*>(p.h)[(int64_t)u * KP + e] : make_float2(0.f, 0.f);
+  for (int sgi = 0; sgi + 1 < p.split_S; ++sgi) {
+    const int64_t slot = (int64_t)u * p.split_S + sgi;
+    const float2 a = p.seg_alpha[slot * K2 + k];
+    const float2 z = reinterpret_cast<const float2*>(p.seg_h)[slot * KP + e];
+    h = make_float2(fmaf(a.x, h.x, fmaf(-a.y, h.y, z.x)), fmaf(a.x, h.y, fmaf(a.y, h.x, z.y)));
+    reinterpret_cast<float2*>(p.xh)[(slot + 1) * KP + e] = h;
+  }
+}
+
 // fixed: caller-provided scratch (fixed_bytes long) for the handover slots
 // instead of the pool; a request that needs more is refused.
 template <int N, int R, int Q, bool RE>
@@ -1278,6 +1378,62 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;
   const int units = nseq * H;
+  // Split schedule: with fewer units than SMs (one long sequence of a few
+  // heads), one CTA per unit leaves most SMs idle.  Each unit is cut into S
+  // segments instead.  A state-only pass gives every segment's own final
+  // state and total decay/rotation (all segments in parallel, no y), a small
+  // kernel chains them into each segment's exact initial state, and the full
+  // pass runs every segment from it.  At least four chunks per segment; not
+  // for packed batches or the no-allocation entry point.
+  {
+    int dv = 0, nsm_s = 0;
+    const int64_t nch = (a->seqlen + Q - 1) / Q;
+    if (!fixed && !a->cu_seqlens && a->seqlen > 0 && cudaGetDevice(&dv) == cudaSuccess &&
+        cudaDeviceGetAttribute(&nsm_s, cudaDevAttrMultiProcessorCount, dv) == cudaSuccess && units < nsm_s) {
+      int S = nsm_s / units;
+      if (S > nch / 4) S = (int)(nch / 4);
+      if (S >= 2) {
+        const int len = (int)((nch + S - 1) / S);
+        S = (int)((nch + len - 1) / len);
+        const size_t nslot = (size_t)units * S;
+        const size_t hb = nslot * (size_t)(N / 2) * 64 * 2 * 4;
+        size_t off = 0;
+        auto take = [&](size_t bytes) {
+          const size_t o = off;
+          off += (bytes + 255) / 256 * 256;
+          return o;
+        };
+        const size_t o_flag = take(nslot * 4), o_xh = take(hb), o_xB = take(nslot * R * N * 2),
+                     o_xx = take(nslot * R * 64 * 2), o_sh = take(hb), o_sa = take(nslot * (N / 2) * 8);
+        const size_t bytes = off;
+        cudaMemPool_t pool = handover_pool(dv);
+        void* buf = nullptr;
+        auto kso = chunked_prefill_kernel<N, R, Q, RE, true>;
+        if (pool && cudaFuncSetAttribute(kso, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) == cudaSuccess &&
+            cudaMallocFromPoolAsync(&buf, bytes, pool, s) == cudaSuccess) {
+          uint8_t* b8 = static_cast<uint8_t*>(buf);
+          p.split_S = S;
+          p.split_len = len;
+          p.xflag = reinterpret_cast<int*>(b8 + o_flag);
+          p.xh = reinterpret_cast<float*>(b8 + o_xh);
+          p.xB = reinterpret_cast<__nv_bfloat16*>(b8 + o_xB);
+          p.xx = reinterpret_cast<__nv_bfloat16*>(b8 + o_xx);
+          p.seg_h = reinterpret_cast<float*>(b8 + o_sh);
+          p.seg_alpha = reinterpret_cast<float2*>(b8 + o_sa);
+          split_prep_kernel<N, R, Q><<<(unsigned)nslot, 256, 0, s>>>(p);
+          kso<<<(unsigned)nslot, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+          const int64_t nel = (int64_t)units * (N / 2) * 64;
+          split_combine_kernel<N><<<(unsigned)((nel + 255) / 256), 256, 0, s>>>(p, units);
+          kern<<<(unsigned)nslot, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+          const cudaError_t e = cudaGetLastError();
+          const cudaError_t ef = cudaFreeAsync(buf, s);
+          record_launch(M3_TEST_KERNEL_CHUNKED_SPLIT, (int)nslot, (long long)bytes);
+          return (e == cudaSuccess && ef == cudaSuccess) ? M3_OK : M3_ERR_CUDA;
+        }
+        cudaGetLastError();  // no pool memory: the one-CTA-per-unit launch below
+      }
+    }
+  }
   // Balanced schedule: with more units than SMs, one CTA per unit leaves the
   // last wave partly empty (256 units on 148 SMs: the second wave is 73 %
   // full).  Instead every SM gets an equal range of the chunks, cutting at
