@@ -224,12 +224,12 @@ struct CtaAbort {
 // on one SM, and instruction fetch is a shared resource: every copy of code
 // that is executed each chunk costs instruction-cache capacity.
 __device__ __noinline__ bool wait_or_abort_slow(uint32_t bar, uint32_t parity, volatile CtaAbort* ab) {
-  const uint64_t t0 = globaltimer_ns(), limit = ab->limit_ns;
+  const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kMaxPolls; ++i) {
     if (umma::mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (ab->flag) return false;
-      if (globaltimer_ns() - t0 > limit) break;
+      if (globaltimer_ns() - t0 > ab->limit_ns) break;
     }
   }
   ab->flag = 1;
@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   // prologue scratch
   __shared__ float sDt[Q + 1], sBet[Q + 1], sWarpTot[4];
   __shared__ float sPsum[G][K2];
-  __shared__ float sPhi[K2];  // cumulative angle per pair at the end of the last chunk, in [-pi, pi)
+  // cumulative angle per pair at the start of chunk c, in [-pi, pi): buffer c & 1
+  // (chunk c writes the next chunk's while others may still read its own)
+  __shared__ float sPhi[2][K2];
   __shared__ float sBScl[MR], sCScl[MR];  // BC norm: 1 / rms of each (token, rank) row of the tile
   __shared__ float sCarryScl[8];          // BC norm of the carried B rows at a segment start
   __shared__ float sPhiEndX[XB][K2];  // the same after chunk c (slot c % XB), for the state warps
@@ -432,12 +434,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // must stay 0, not become softplus(bias))
     constexpr uint32_t kNoToken = 0xFFFFFFFFu;
     const bool dt_sp = (p.pro & M3_PRO_DT_SOFTPLUS) != 0;
-    auto load_scalars = [&](int c, uint32_t& d, uint32_t& l) {
+    auto load_scalars = [&](int c, uint32_t& d, uint32_t& l, int tok) {
       d = dt_sp ? kNoToken : 0u;
       l = 0u;
-      if (pt <= Q && c < nchunks) {
+      if (tok <= Q && c < nchunks) {
         const int si = seg_of(c);
-        const int64_t i = (int64_t)(c - sSegC0[si]) * Q + pt;
+        const int64_t i = (int64_t)(c - sSegC0[si]) * Q + tok;
         if (i < seg_ntok(si)) {
           const int64_t row = (sSegTok0[si] + i) * H + seg_head(si);
           d = __ldg(dt_bits + row);
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       }
     };
     uint32_t d_cur, l_cur;
-    load_scalars(0, d_cur, l_cur);
+    load_scalars(0, d_cur, l_cur, pt);
     // prologue of chunk c: scalars, angle scan, rotation of B and C, X and W X.
     // Returns false when the pipeline was aborted.
     auto prologue = [&](int c, auto normtag) -> bool {
@@ -457,13 +459,17 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const float A = sSegA[si];
       // a segment starts from the phase 0 (its initial state is un-rotated);
       // these threads also wrote the previous chunk's phase
-      if (c == sSegC0[si] && pt < K2) sPhi[pt] = 0.f;
+      const int pb = c & 1;  // this chunk's phase buffer
+      if (c == sSegC0[si] && pt < K2) sPhi[pb][pt] = 0.f;
       uint32_t d_nxt, l_nxt;
-      load_scalars(c + 1, d_nxt, l_nxt);
+      load_scalars(c + 1, d_nxt, l_nxt, pt);
       bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       // scalar slot xs last served chunk c - XB: its output must be done
       if (got && c >= XB) got = wait_xfree(c - XB);
-      if (!group_and(1, NPRO, got)) return false;
+      // Every thread waited itself.  The vote on `got` is taken at the
+      // chunk's closing barrier: a thread whose wait gave up computes on
+      // whatever the tiles hold (no fault, no wait) and the group leaves
+      // there together; one barrier fewer per chunk.
       if constexpr (NORM) {
         // ---- BC norm: 1 / rms of every B and C row (token, rank) of the tile
         //      as it landed; TPR adjacent threads per row, 16-byte chunks
@@ -509,7 +515,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         }
         if (lane == 31) sWarpTot[warp] = v;
       }
-      group_sync(1, NPRO);
+      group_sync(1, NPRO);  // (also: sDt complete for the angle scan)
       if (pt < Q) {
         for (int w = 0; w < warp; ++w) v += sWarpTot[w];
         sLam[xs][pt] = v;
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         if (pt == 0) sLamEnd[xs] = lam_end;
       }
       if (RE && g == 0) {  // theta = 0: the phase stays 0
-        sPhiEndX[xs][k] = sPhi[k];
+        sPhiEndX[xs][k] = sPhi[pb][k];
         mbar_arrive_warp(saddr(&bar_phend[xs]));
       }
       // ---- angle scan, part 2, and the in-place rotation of B and C by
@@ -555,12 +561,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           for (int r = 0; r < R; ++r) {
             const uint32_t rc = sw128_offset(i * R + r, col);
             const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
+            // (both loads before the stores: the stores may alias them for the compiler)
             const float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
+            const float2 cc = SO ? make_float2(0.f, 0.f) : bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
             *reinterpret_cast<uint32_t*>(Bt + ob) = pack_half2(b.x, b.y);
-            if (!SO) {
-              const float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
-              *reinterpret_cast<uint32_t*>(Ct + o) = pack_half2(cc.x, cc.y);
-            }
+            if (!SO) *reinterpret_cast<uint32_t*>(Ct + o) = pack_half2(cc.x, cc.y);
           }
         }
       } else {
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           off += (gg < g) ? sv : 0.f;
           tot += sv;
         }
-        const float ph_end = sPhi[k] + tot;
+        const float ph_end = sPhi[pb][k] + tot;
         uint8_t* Bt = stg + Cfg::OFF_B;
         uint8_t* Ct = stg + Cfg::OFF_C;
         uint8_t* Blo = stg + Cfg::OFF_BLO;
@@ -582,7 +587,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         // then the rotations: independent work the scheduler can overlap
         float cs[TPG], sn[TPG];
         {
-          float phi = sPhi[k] + off;
+          float phi = sPhi[pb][k] + off;
 #pragma unroll
           for (int ii = 0; ii < TPG; ++ii) {
             phi += om[ii];
@@ -598,23 +603,25 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           for (int r = 0; r < R; ++r) {
             const uint32_t rc = sw128_offset(i * R + r, col);
             const uint32_t o = blk * (MR * 128) + rc, ob = blk * Cfg::BB + rc;
+            // (both loads before the stores: the stores may alias them for
+            // the compiler; the state-only pass has no C)
             float2 b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Bt + ob));
+            float2 cc = SO ? make_float2(0.f, 0.f) : bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
             if constexpr (NORM) {
               const float fb = sBScl[i * R + r];
               b.x *= fb;
               b.y *= fb;
+              if (!SO) {
+                const float fc = sCScl[i * R + r];
+                cc.x *= fc;
+                cc.y *= fc;
+              }
             }
             uint32_t hi, lo;
             split_half2(cs[ii] * b.x - sn[ii] * b.y, sn[ii] * b.x + cs[ii] * b.y, hi, lo);
             *reinterpret_cast<uint32_t*>(Bt + ob) = hi;
             *reinterpret_cast<uint32_t*>(Blo + ob) = lo;
-            if (!SO) {  // (the state-only pass has no C)
-              float2 cc = bf2_to_f2(*reinterpret_cast<const uint32_t*>(Ct + o));
-              if constexpr (NORM) {
-                const float fc = sCScl[i * R + r];
-                cc.x *= fc;
-                cc.y *= fc;
-              }
+            if (!SO) {
               split_half2(cs[ii] * cc.x - sn[ii] * cc.y, sn[ii] * cc.x + cs[ii] * cc.y, hi, lo);
               *reinterpret_cast<uint32_t*>(Ct + o) = hi;
               *reinterpret_cast<uint32_t*>(Clo + o) = lo;
@@ -626,10 +633,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           mbar_arrive_warp(saddr(&bar_phend[xs]));
         }
       }
-      group_sync(1, NPRO);  // sDw ready; theta and sPhi fully read
-      if (g == 0) sPhi[k] = sPhiEndX[xs][k];  // advance the running phase (same thread wrote it)
+      // the next chunk's running phase, in the other buffer (the same thread
+      // wrote sPhiEndX); the closing barrier orders it, sDw and the last
+      // reads of theta before the stage goes to the state warps and MMAs
+      if (g == 0) sPhi[pb ^ 1][k] = sPhiEndX[xs][k];
       fence_async_smem();
-      group_sync(1, NPRO);
+      if (!group_and(1, NPRO, got)) return false;
       if (pt == 0) mbar_arrive(saddr(&bar_opready[s]));
       d_cur = d_nxt;
       l_cur = l_nxt;
@@ -642,7 +651,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       bool got = wait_or_abort(saddr(&bar_sfull[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       if (got && c >= 1)
         got = wait_or_abort(saddr(&bar_yfull[(c - 1) & 1]), (uint32_t)(((c - 1) >> 1) & 1), abort_flag);
-      if (!group_and(1, NPRO, got)) return false;
+      // (the vote on `got` is taken at the closing barrier, as in the prologue)
       tc_fence_after();
       // warp w covers accumulator rows 16(w%4) .. +15 (TMEM lane quarter w%4)
       // and one slice of CPH columns; with the 16x256b shape thread `lane`
@@ -705,7 +714,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       }
       tc_fence_before();
       fence_async_smem();
-      group_sync(1, NPRO);
+      if (!group_and(1, NPRO, got)) return false;
       if (pt == 0) mbar_arrive(saddr(&bar_spready));
       return true;
     };
