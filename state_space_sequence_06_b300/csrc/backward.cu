@@ -185,7 +185,7 @@ m3_status chunked_go(const m3_backward_args* a, const void* const in[8], int G, 
   take(9, bc_head);                               // per-head dB
   take(10, bc_head);                              // per-head dC
   if (tot > (size_t(16) << 30)) return M3_ERR_UNSUPPORTED;
-  const size_t smem1 = sizeof(float) * (2 * MR * NS + 2 * MR * PS + Q * K);
+  const size_t smem1 = sizeof(float) * (2 * MR * NS + 2 * MR * PS);  // (the angles share the dy tile)
   const size_t smem3 = sizeof(float) * (2 * MR * NS + 2 * MR * PS + 2 * NN * PS + 2 * MR * MS + Q * K);
   auto k1 = chunk_sums_kernel<T, NN, RR>;
   auto k3 = chunk_grads_kernel<T, NN, RR>;

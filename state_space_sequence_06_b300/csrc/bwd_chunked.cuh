@@ -205,24 +205,36 @@ __device__ __forceinline__ void chunk_prologue(const ChunkBwdParams& p, int64_t 
   __syncthreads();
 }
 
-// Rows of the chunk's B (or C) rotated by e^{-i phi_t} into dst[MR][NS]
-// (zero rows past the chunk's end).
+// sin and cos of an angle of at most a few tens of radians: one reduction
+// by 2 pi (rounded quotient), then the special-function unit on [-pi, pi].
+__device__ __forceinline__ void sincos_angle(float x, float* s, float* c) {
+  const float q = rintf(x * 0.15915494309189535f);
+  __sincosf(fmaf(-q, 6.283185307179586f, x), s, c);
+}
+
+// Rows of the chunk's B and C rotated by e^{-i phi_t} into Bt, Ct [MR][NS]
+// (zero rows past the chunk's end); one sine and cosine per (token, pair).
 template <typename T, int R, int N, int K, int MR, int NS, int NT>
-__device__ __forceinline__ void load_rotated(const void* src, int64_t tok0, int G, int grp, int n, const float* phi,
-                                             float* dst) {
+__device__ __forceinline__ void load_rotated(const void* Bsrc, const void* Csrc, int64_t tok0, int G, int grp, int n,
+                                             const float* phi, float* Bt, float* Ct) {
   for (int i = threadIdx.x; i < MR * K; i += NT) {
     const int m = i / K, k = i % K, t = m / R, r = m % R;
-    float re = 0.f, im = 0.f;
+    float bre = 0.f, bim = 0.f, cre = 0.f, cim = 0.f;
     if (t < n) {
       const int64_t o = (((tok0 + t) * G + grp) * R + r) * N + 2 * k;
-      const float br = ldv<T>(src, o), bi = ldv<T>(src, o + 1);
+      const float br = ldv<T>(Bsrc, o), bi = ldv<T>(Bsrc, o + 1);
+      const float cr = ldv<T>(Csrc, o), ci = ldv<T>(Csrc, o + 1);
       float sn, cs;
-      sincosf(phi[t * K + k], &sn, &cs);
-      re = br * cs + bi * sn;  // e^{-i phi} (br + i bi)
-      im = bi * cs - br * sn;
+      sincos_angle(phi[t * K + k], &sn, &cs);
+      bre = br * cs + bi * sn;  // e^{-i phi} (br + i bi)
+      bim = bi * cs - br * sn;
+      cre = cr * cs + ci * sn;
+      cim = ci * cs - cr * sn;
     }
-    dst[m * NS + 2 * k] = re;
-    dst[m * NS + 2 * k + 1] = im;
+    Bt[m * NS + 2 * k] = bre;
+    Bt[m * NS + 2 * k + 1] = bim;
+    Ct[m * NS + 2 * k] = cre;
+    Ct[m * NS + 2 * k + 1] = cim;
   }
 }
 
@@ -251,9 +263,11 @@ __global__ void __launch_bounds__(256) chunk_sums_kernel(const ChunkBwdParams p)
   float* Ct = Bt + MR * NS;      // [MR][NS]
   float* Xf = Ct + MR * NS;      // [MR][PS]: f_t x_t
   float* Ye = Xf + MR * PS;      // [MR][PS]: e^{Lam_t} dy_t
-  float* phi = Ye + MR * PS;     // [Q][K]
+  float* phi = Ye;               // [Q][K] angles, until dy is loaded (Q K <= MR PS)
+  static_assert(Q * K <= MR * PS, "angles fit in the dy tile");
   __shared__ ChunkScalars<Q> s;
   __shared__ float sred[32];
+  __shared__ float sPhiEnd[K];
 
   const int c = blockIdx.x % p.nch, unit = blockIdx.x / p.nch;  // chunk c of unit `unit`
   const int b = unit / p.H, head = unit % p.H, grp = head / (p.H / p.G);
@@ -261,9 +275,10 @@ __global__ void __launch_bounds__(256) chunk_sums_kernel(const ChunkBwdParams p)
   const int n = (int)((p.L - (int64_t)c * Q) < Q ? (p.L - (int64_t)c * Q) : Q);
   const float A = p.A[head];
   chunk_prologue<T, Q, K, NT>(p, tok0, head, n, A, s, phi, sred);
-  load_rotated<T, R, N, K, MR, NS, NT>(p.B, tok0, p.G, grp, n, phi, Bt);
-  load_rotated<T, R, N, K, MR, NS, NT>(p.C, tok0, p.G, grp, n, phi, Ct);
+  load_rotated<T, R, N, K, MR, NS, NT>(p.B, p.C, tok0, p.G, grp, n, phi, Bt, Ct);
   load_rows<T, R, P, MR, PS, NT>(static_cast<const T*>(p.x), tok0, p.H, head, n, s.f, Xf);
+  for (int k = threadIdx.x; k < K; k += NT) sPhiEnd[k] = phi[(n - 1) * K + k];
+  __syncthreads();  // the angles are read: dy goes over them
   load_rows<float, R, P, MR, PS, NT>(p.dy, tok0, p.H, head, n, s.eL, Ye);
   __syncthreads();
 
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(256) chunk_sums_kernel(const ChunkBwdParams p)
     for (int i = 0; i < TM; ++i) {
       const int row = ty + 16 * i, k = row >> 1;
       float sn, cs;
-      sincosf(phi[(n - 1) * K + k], &sn, &cs);
+      sincos_angle(sPhiEnd[k], &sn, &cs);
 #pragma unroll
       for (int j = 0; j < TN; ++j) {
         const float mine = acc[i][j], other = __shfl_xor_sync(0xffffffffu, mine, 16);
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(256) chunk_sums_kernel(const ChunkBwdParams p)
   if (threadIdx.x < K) {
     const int k = threadIdx.x;
     float sn, cs;
-    sincosf(phi[(n - 1) * K + k], &sn, &cs);
+    sincosf(sPhiEnd[k], &sn, &cs);
     const float e = expf(s.Lam[n - 1]);
     p.alpha[(int64_t)unit * p.nch * K + (int64_t)c * K + k] = make_float2(e * cs, e * sn);
   }
@@ -417,8 +432,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
   const int KP = K * P;
 
   chunk_prologue<T, Q, K, NT>(p, tok0, head, n, A, s, phi, sred);
-  load_rotated<T, R, N, K, MR, NS, NT>(p.B, tok0, p.G, grp, n, phi, Bt);
-  load_rotated<T, R, N, K, MR, NS, NT>(p.C, tok0, p.G, grp, n, phi, Ct);
+  load_rotated<T, R, N, K, MR, NS, NT>(p.B, p.C, tok0, p.G, grp, n, phi, Bt, Ct);
   load_rows<T, R, P, MR, PS, NT>(static_cast<const T*>(p.x), tok0, p.H, head, n, nullptr, X);
   load_rows<float, R, P, MR, PS, NT>(p.dy, tok0, p.H, head, n, nullptr, dY);
   {
@@ -432,7 +446,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
       Gs[(2 * k) * PS + q] = h.x;
       Gs[(2 * k + 1) * PS + q] = h.y;
       float sn, cs;
-      sincosf(phi[(n - 1) * K + k], &sn, &cs);
+      sincos_angle(phi[(n - 1) * K + k], &sn, &cs);
       dG[(2 * k) * PS + q] = g.x * cs + g.y * sn;  // e^{-i phi_end} g
       dG[(2 * k + 1) * PS + q] = g.y * cs - g.x * sn;
       // (P = 64: the two warps of one k reduce separately)
@@ -613,7 +627,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
         }
         if (t < n) {
           float sn, cs;
-          sincosf(phi[t * K + k], &sn, &cs);
+          sincos_angle(phi[t * K + k], &sn, &cs);
           const float v = (tx & 1) ? fmaf(dre, sn, dim * cs) : fmaf(dre, cs, -dim * sn);
           dst_base[((tok0 + t) * p.GB + (p.GB == p.H ? head : grp)) * (R * N) + (m % R) * N + col] = v;
         }
