@@ -89,6 +89,24 @@ __device__ __forceinline__ float ldv(const void* p, int64_t i) {
   return to_f(static_cast<const T*>(p)[i]);
 }
 
+// Elements i and i + 1 (i even) in one read-only load.
+template <typename T>
+__device__ __forceinline__ float2 ld_pair(const void* p, int64_t i);
+template <>
+__device__ __forceinline__ float2 ld_pair<float>(const void* p, int64_t i) {
+  return __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(p) + i));
+}
+template <>
+__device__ __forceinline__ float2 ld_pair<__nv_bfloat16>(const void* p, int64_t i) {
+  const unsigned w = __ldg(reinterpret_cast<const unsigned*>(static_cast<const __nv_bfloat16*>(p) + i));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Loads of the per-chunk loaders go out U iterations at a time (all loads of
+// a batch before its shared-memory stores), so that several are in flight
+// per thread: one CTA per SM holds few warps to hide their latency.
+constexpr int kLoadBatch = 4;
+
 // Block-wide C (+)= A * B over shared memory, 256 threads as (ty, tx) in
 // 16 x 16: the thread owns rows ty + 16 i (i < TM) and columns tx + 16 j
 // (j < TN).  a(m, k) and b(k, n) read the operands.
@@ -173,9 +191,23 @@ __device__ __forceinline__ void chunk_prologue(const ChunkBwdParams& p, int64_t 
     if (tid < Q) s.Lam[tid] = v;
   }
   // theta of the chunk's tokens, staged for the angle scan
-  for (int i = tid; i < Q * K; i += NT) {
-    const int t = i / K;
-    phi[i] = (t < n && p.theta) ? ldv<T>(p.theta, (tok0 + t) * p.H * K + (int64_t)head * K + i % K) : 0.f;
+  for (int i0 = tid; i0 < Q * K / 2; i0 += NT * kLoadBatch) {
+    float2 v[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, t = (2 * i) / K;
+      v[u] = (i < Q * K / 2 && t < n && p.theta)
+                 ? ld_pair<T>(p.theta, (tok0 + t) * p.H * K + (int64_t)head * K + (2 * i) % K)
+                 : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT;
+      if (i < Q * K / 2) {
+        phi[2 * i] = v[u].x;
+        phi[2 * i + 1] = v[u].y;
+      }
+    }
   }
   __syncthreads();
   if (tid < Q) {
@@ -217,24 +249,30 @@ __device__ __forceinline__ void sincos_angle(float x, float* s, float* c) {
 template <typename T, int R, int N, int K, int MR, int NS, int NT>
 __device__ __forceinline__ void load_rotated(const void* Bsrc, const void* Csrc, int64_t tok0, int G, int grp, int n,
                                              const float* phi, float* Bt, float* Ct) {
-  for (int i = threadIdx.x; i < MR * K; i += NT) {
-    const int m = i / K, k = i % K, t = m / R, r = m % R;
-    float bre = 0.f, bim = 0.f, cre = 0.f, cim = 0.f;
-    if (t < n) {
-      const int64_t o = (((tok0 + t) * G + grp) * R + r) * N + 2 * k;
-      const float br = ldv<T>(Bsrc, o), bi = ldv<T>(Bsrc, o + 1);
-      const float cr = ldv<T>(Csrc, o), ci = ldv<T>(Csrc, o + 1);
-      float sn, cs;
-      sincos_angle(phi[t * K + k], &sn, &cs);
-      bre = br * cs + bi * sn;  // e^{-i phi} (br + i bi)
-      bim = bi * cs - br * sn;
-      cre = cr * cs + ci * sn;
-      cim = ci * cs - cr * sn;
+  for (int i0 = threadIdx.x; i0 < MR * K; i0 += NT * kLoadBatch) {
+    float2 bv[kLoadBatch], cv[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, m = i / K, k = i % K, t = m / R, r = m % R;
+      bv[u] = cv[u] = make_float2(0.f, 0.f);
+      if (i < MR * K && t < n) {
+        const int64_t o = (((tok0 + t) * G + grp) * R + r) * N + 2 * k;
+        bv[u] = ld_pair<T>(Bsrc, o);
+        cv[u] = ld_pair<T>(Csrc, o);
+      }
     }
-    Bt[m * NS + 2 * k] = bre;
-    Bt[m * NS + 2 * k + 1] = bim;
-    Ct[m * NS + 2 * k] = cre;
-    Ct[m * NS + 2 * k + 1] = cim;
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, m = i / K, k = i % K, t = m / R;
+      if (i >= MR * K) break;
+      float sn = 0.f, cs = 1.f;
+      if (t < n) sincos_angle(phi[t * K + k], &sn, &cs);
+      const float2 b = bv[u], c = cv[u];
+      Bt[m * NS + 2 * k] = b.x * cs + b.y * sn;  // e^{-i phi} (b.x + i b.y)
+      Bt[m * NS + 2 * k + 1] = b.y * cs - b.x * sn;
+      Ct[m * NS + 2 * k] = c.x * cs + c.y * sn;
+      Ct[m * NS + 2 * k + 1] = c.y * cs - c.x * sn;
+    }
   }
 }
 
@@ -243,11 +281,22 @@ __device__ __forceinline__ void load_rotated(const void* Bsrc, const void* Csrc,
 template <typename T, int R, int P, int MR, int PS, int NT>
 __device__ __forceinline__ void load_rows(const T* src, int64_t tok0, int H, int head, int n, const float* scale,
                                           float* dst) {
-  for (int i = threadIdx.x; i < MR * P; i += NT) {
-    const int m = i / P, q = i % P, t = m / R;
-    float v = 0.f;
-    if (t < n) v = to_f(src[((tok0 + t) * H + head) * (R * P) + (m % R) * P + q]) * (scale ? scale[t] : 1.f);
-    dst[m * PS + q] = v;
+  for (int i0 = threadIdx.x; i0 < MR * P / 2; i0 += NT * kLoadBatch) {
+    float2 v[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, m = (2 * i) / P, q = (2 * i) % P, t = m / R;
+      v[u] = (i < MR * P / 2 && t < n) ? ld_pair<T>(src, ((tok0 + t) * H + head) * (R * P) + (m % R) * P + q)
+                                       : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, m = (2 * i) / P, q = (2 * i) % P, t = m / R;
+      if (i >= MR * P / 2) break;
+      const float sc = (scale && t < n) ? scale[t] : 1.f;
+      dst[m * PS + q] = v[u].x * sc;
+      dst[m * PS + q + 1] = v[u].y * sc;
+    }
   }
 }
 
@@ -440,20 +489,32 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
     const float2* hs = p.Hs + ((int64_t)unit * (p.nch + 1) + c) * KP;
     const float2* he = hs + KP;
     const float2* dhe = p.dHe + ((int64_t)unit * p.nch + c) * KP;
-    for (int e = tid; e < KP; e += NT) {
-      const int k = e / P, q = e % P;
-      const float2 h = hs[e], g = dhe[e], hn = he[e];
-      Gs[(2 * k) * PS + q] = h.x;
-      Gs[(2 * k + 1) * PS + q] = h.y;
-      float sn, cs;
-      sincos_angle(phi[(n - 1) * K + k], &sn, &cs);
-      dG[(2 * k) * PS + q] = g.x * cs + g.y * sn;  // e^{-i phi_end} g
-      dG[(2 * k + 1) * PS + q] = g.y * cs - g.x * sn;
-      // (P = 64: the two warps of one k reduce separately)
-      float v = -(g.x * hn.y - g.y * hn.x);
+    static_assert((K * P) % (NT * kLoadBatch) == 0, "whole batches of state elements");
+    for (int e0 = tid; e0 < KP; e0 += NT * kLoadBatch) {
+      float2 hb[kLoadBatch], gb[kLoadBatch], nb[kLoadBatch];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) sPhiEndPart[k][(q >> 5) & 1] = v;
+      for (int u = 0; u < kLoadBatch; ++u) {
+        hb[u] = __ldg(hs + e0 + u * NT);
+        gb[u] = __ldg(dhe + e0 + u * NT);
+        nb[u] = __ldg(he + e0 + u * NT);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int e = e0 + u * NT;
+        const int k = e / P, q = e % P;
+        const float2 h = hb[u], g = gb[u], hn = nb[u];
+        Gs[(2 * k) * PS + q] = h.x;
+        Gs[(2 * k + 1) * PS + q] = h.y;
+        float sn, cs;
+        sincos_angle(phi[(n - 1) * K + k], &sn, &cs);
+        dG[(2 * k) * PS + q] = g.x * cs + g.y * sn;  // e^{-i phi_end} g
+        dG[(2 * k + 1) * PS + q] = g.y * cs - g.x * sn;
+        // (P = 64: the two warps of one k reduce separately)
+        float v = -(g.x * hn.y - g.y * hn.x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) sPhiEndPart[k][(q >> 5) & 1] = v;
+      }
     }
   }
   if (tid < Q) {
