@@ -221,7 +221,7 @@ m3_status chunked_go(const m3_backward_args* a, const void* const in[8], int G, 
   k1<<<chunks, Cfg::NT, smem1, s>>>(p);
   const unsigned bpu = (unsigned)((KP + 255) / 256);
   chunk_scan_kernel<T><<<(unsigned)(units * bpu), 256, 0, s>>>(p, RR, NN, P);
-  k3<<<chunks, Cfg::NT, smem3, s>>>(p);
+  k3<<<chunks, Cfg::NTG, smem3, s>>>(p);
   unit_final_kernel<T><<<(unsigned)units, 256, 0, s>>>(p, RR, NN, P, Q);
   head_sums_kernel<<<H, 256, 0, s>>>(p.dA_part, p.dD_part, a->dims.batch, H, nch, a->dA, a->dD);
   if (grouped) {

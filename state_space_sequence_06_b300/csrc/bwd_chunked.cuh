@@ -107,17 +107,17 @@ __device__ __forceinline__ float2 ld_pair<__nv_bfloat16>(const void* p, int64_t 
 // per thread: one CTA per SM holds few warps to hide their latency.
 constexpr int kLoadBatch = 4;
 
-// Block-wide C (+)= A * B over shared memory, 256 threads as (ty, tx) in
-// 16 x 16: the thread owns rows ty + 16 i (i < TM) and columns tx + 16 j
-// (j < TN).  a(m, k) and b(k, n) read the operands.
-template <int TM, int TN, class FA, class FB>
+// Block-wide C (+)= A * B over shared memory, the block's threads as (ty,
+// tx) in TY x 16: the thread owns rows ty + TY i (i < TM) and columns
+// tx + 16 j (j < TN).  a(m, k) and b(k, n) read the operands.
+template <int TM, int TN, int TY = 16, class FA, class FB>
 __device__ __forceinline__ void block_mm(float (&acc)[TM][TN], int K, FA a, FB b) {
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
 #pragma unroll 2
   for (int k = 0; k < K; ++k) {
     float av[TM], bv[TN];
 #pragma unroll
-    for (int i = 0; i < TM; ++i) av[i] = a(ty + 16 * i, k);
+    for (int i = 0; i < TM; ++i) av[i] = a(ty + TY * i, k);
 #pragma unroll
     for (int j = 0; j < TN; ++j) bv[j] = b(k, tx + 16 * j);
 #pragma unroll
@@ -147,7 +147,9 @@ template <int N_, int R_>
 struct BwdCfg {
   static constexpr int N = N_, R = R_, P = 64, MR = 64, Q = MR / R, K = N / 2;
   static constexpr int NS = N + 1, PS = P + 1, MS = MR + 1;  // odd row strides
-  static constexpr int NT = 256;
+  static constexpr int NT = 256;   // chunk sums (two CTAs per SM)
+  static constexpr int NTG = 512;  // chunk gradients (one CTA per SM: more warps to hide latency)
+  static constexpr int TYG = NTG / 16, TQG = MR / TYG;  // its thread rows, and rows per thread
 };
 
 // Per-chunk scalars, shared by the two per-chunk kernels.
@@ -449,10 +451,10 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(const ChunkBwdParams p,
 // ------------------------------------------------------------------ phase 3
 
 template <typename T, int N_, int R_>
-__global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParams p) {
+__global__ void __launch_bounds__(BwdCfg<N_, R_>::NTG, 1) chunk_grads_kernel(const ChunkBwdParams p) {
   using Cfg = BwdCfg<N_, R_>;
   constexpr int N = Cfg::N, R = Cfg::R, P = Cfg::P, MR = Cfg::MR, Q = Cfg::Q, K = Cfg::K;
-  constexpr int NS = Cfg::NS, PS = Cfg::PS, MS = Cfg::MS, NT = Cfg::NT;
+  constexpr int NS = Cfg::NS, PS = Cfg::PS, MS = Cfg::MS, NT = Cfg::NTG, TY = Cfg::TYG;
   extern __shared__ float sm[];
   float* Bt = sm;               // [MR][NS] rotated B rows
   float* Ct = Bt + MR * NS;     // [MR][NS] rotated C rows
@@ -540,16 +542,16 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
   };
 
   // ---- P1: S = Ct Bt^T and dM = dY X^T (MR x MR), their products with EW
-  constexpr int TQ = MR / 16;
-  float accS[TQ][TQ], accM[TQ][TQ];
+  constexpr int TQ = Cfg::TQG, TC = MR / 16;  // rows and columns of an MR x MR tile per thread
+  float accS[TQ][TC], accM[TQ][TC];
   zero_acc(accS);
   zero_acc(accM);
-  block_mm<TQ, TQ>(accS, N, [&](int m, int k) { return Ct[m * NS + k]; }, [&](int k, int j) { return Bt[j * NS + k]; });
-  block_mm<TQ, TQ>(accM, P, [&](int m, int k) { return dY[m * PS + k]; }, [&](int k, int j) { return X[j * PS + k]; });
+  block_mm<TQ, TC, TY>(accS, N, [&](int m, int k) { return Ct[m * NS + k]; }, [&](int k, int j) { return Bt[j * NS + k]; });
+  block_mm<TQ, TC, TY>(accM, P, [&](int m, int k) { return dY[m * PS + k]; }, [&](int k, int j) { return X[j * PS + k]; });
 #pragma unroll
   for (int i = 0; i < TQ; ++i)
 #pragma unroll
-    for (int j = 0; j < TQ; ++j) T1[(ty + 16 * i) * MS + tx + 16 * j] = accM[i][j] * accS[i][j];
+    for (int j = 0; j < TC; ++j) T1[(ty + TY * i) * MS + tx + 16 * j] = accM[i][j] * accS[i][j];
   __syncthreads();
   // dEW_tj = sum over rank pairs of dM * S; a_tj = dEW EW, b_tj = dEW E (t > j)
   float* ewa = (R == 1) ? T2 : sEWa;
@@ -589,8 +591,8 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
 #pragma unroll
   for (int i = 0; i < TQ; ++i)
 #pragma unroll
-    for (int j = 0; j < TQ; ++j) {
-      const int m = ty + 16 * i, m2 = tx + 16 * j;
+    for (int j = 0; j < TC; ++j) {
+      const int m = ty + TY * i, m2 = tx + 16 * j;
       float E;
       const float ew = ew_of(m / R, m2 / R, E);
       T2[m * MS + m2] = accS[i][j] * ew;
@@ -604,10 +606,10 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
     constexpr int TP = P / 16;
     float acc[TQ][TP];
     zero_acc(acc);
-    block_mm<TQ, TP>(acc, N, [&](int m, int k) { return Ct[m * NS + k]; }, [&](int k, int q) { return Gs[k * PS + q]; });
+    block_mm<TQ, TP, TY>(acc, N, [&](int m, int k) { return Ct[m * NS + k]; }, [&](int k, int q) { return Gs[k * PS + q]; });
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
-      const int m = ty + 16 * i;
+      const int m = ty + TY * i;
       float v = 0.f;
 #pragma unroll
       for (int j = 0; j < TP; ++j) v = fmaf(dY[m * PS + tx + 16 * j], acc[i][j], v);
@@ -640,12 +642,12 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
     float acc[TQ][TP], acc2[TQ][TP];
     zero_acc(acc);
     zero_acc(acc2);
-    block_mm<TQ, TP>(acc, MR, [&](int m, int k) { return T2[k * MS + m]; }, [&](int k, int q) { return dY[k * PS + q]; });
-    block_mm<TQ, TP>(acc2, N, [&](int m, int k) { return Bt[m * NS + k]; }, [&](int k, int q) { return dG[k * PS + q]; });
+    block_mm<TQ, TP, TY>(acc, MR, [&](int m, int k) { return T2[k * MS + m]; }, [&](int k, int q) { return dY[k * PS + q]; });
+    block_mm<TQ, TP, TY>(acc2, N, [&](int m, int k) { return Bt[m * NS + k]; }, [&](int k, int q) { return dG[k * PS + q]; });
     float dd = 0.f;
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
-      const int m = ty + 16 * i, t = m / R;
+      const int m = ty + TY * i, t = m / R;
       if (t < n) {
         float* dst = p.dx + ((tok0 + t) * p.H + head) * (R * P) + (m % R) * P;
 #pragma unroll
@@ -676,7 +678,7 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
   auto emit = [&](float (&acc)[TQ][TN], const float* rot, float* dst_base, bool first) {
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
-      const int m = ty + 16 * i, t = m / R;
+      const int m = ty + TY * i, t = m / R;
 #pragma unroll
       for (int j = 0; j < TN; ++j) {
         const int col = tx + 16 * j, k = col >> 1;
@@ -701,11 +703,11 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
     float acc[TQ][TN], acc2[TQ][TN];
     zero_acc(acc);
     zero_acc(acc2);
-    block_mm<TQ, TN>(acc, MR, [&](int m, int k) { return T1[m * MS + k]; }, [&](int k, int q) { return Bt[k * NS + q]; });
-    block_mm<TQ, TN>(acc2, P, [&](int m, int k) { return dY[m * PS + k]; }, [&](int k, int q) { return Gs[q * PS + k]; });
+    block_mm<TQ, TN, TY>(acc, MR, [&](int m, int k) { return T1[m * MS + k]; }, [&](int k, int q) { return Bt[k * NS + q]; });
+    block_mm<TQ, TN, TY>(acc2, P, [&](int m, int k) { return dY[m * PS + k]; }, [&](int k, int q) { return Gs[q * PS + k]; });
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
-      const float el = s.eL[(ty + 16 * i) / R];
+      const float el = s.eL[(ty + TY * i) / R];
 #pragma unroll
       for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(el, acc2[i][j], acc[i][j]);
     }
@@ -716,11 +718,11 @@ __global__ void __launch_bounds__(256, 1) chunk_grads_kernel(const ChunkBwdParam
     float acc[TQ][TN], accw[TQ][TN];
     zero_acc(acc);
     zero_acc(accw);
-    block_mm<TQ, TN>(acc, MR, [&](int m, int k) { return T1[k * MS + m]; }, [&](int k, int q) { return Ct[k * NS + q]; });
-    block_mm<TQ, TN>(accw, P, [&](int m, int k) { return X[m * PS + k]; }, [&](int k, int q) { return dG[q * PS + k]; });
+    block_mm<TQ, TN, TY>(acc, MR, [&](int m, int k) { return T1[k * MS + m]; }, [&](int k, int q) { return Ct[k * NS + q]; });
+    block_mm<TQ, TN, TY>(accw, P, [&](int m, int k) { return X[m * PS + k]; }, [&](int k, int q) { return dG[q * PS + k]; });
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
-      const int m = ty + 16 * i;
+      const int m = ty + TY * i;
       const float fv = s.f[m / R];
       float qv = 0.f;
 #pragma unroll
