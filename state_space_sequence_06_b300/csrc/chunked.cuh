@@ -159,6 +159,8 @@ struct ChunkCfg {
   // TMEM columns (f32): S[2], Y[2], Yi[2], state, chunk-local state
   static constexpr int COL_S = 0, COL_Y = 2 * MR, COL_YI = 2 * MR + 2 * P, COL_G = 2 * MR + 4 * P;
   static constexpr int COL_SC = COL_G + P;  // the chunk-local state B^T (W X) of MMA 4
+  // its second buffer in the state-only pass, which has no S, Y or Yi
+  static constexpr int COL_SC1 = COL_S;
   static constexpr int TMEM_COLS = 512;
   static_assert(COL_SC + P <= TMEM_COLS, "TMEM columns");
 };
@@ -268,7 +270,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   // cannot.
   __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB], bar_phend[XB];
-  __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_scfull, bar_scfree, bar_rfree;
+  __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_rfree;
+  // scfull / scfree per chunk-local state buffer: one buffer (index 0) in the
+  // full pass; two in the state-only pass, chunk c in buffer c & 1, so MMA 4
+  // of chunk c + 1 does not wait for the state step of chunk c
+  __shared__ __align__(8) uint64_t bar_scfull[2], bar_scfree[2];
   // mdone[i]: every product MMA thread i issued is complete (its last commit,
   // waited for before the TMEM is freed, also after an abort)
   __shared__ __align__(8) uint64_t bar_mdone[2];
@@ -397,13 +403,15 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       // MMA 2 completion and the output epilogue (SO: the state warps, once
       // the slot's scalars are no longer read)
       mbar_init(saddr(&bar_xfree[x]), SO ? 1 : 2);
-      mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X
+      mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X (not in SO)
       mbar_init(saddr(&bar_phend[x]), K2);  // the phase after the slot's chunk, one arrival per pair
     }
     mbar_init(saddr(&bar_spready), 1);
     mbar_init(saddr(&bar_stready), 1);
-    mbar_init(saddr(&bar_scfull), 1);
-    mbar_init(saddr(&bar_scfree), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(saddr(&bar_scfull[b]), 1);
+      mbar_init(saddr(&bar_scfree[b]), 1);
+    }
     mbar_init(saddr(&bar_rfree), 1);
     mbar_init(saddr(&bar_mdone[0]), 1);
     mbar_init(saddr(&bar_mdone[1]), 1);
@@ -535,6 +543,31 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       }
       group_sync(1, NPRO);  // sLam and sPsum complete
       const float lam_end = sLam[xs][Q - 1];
+      if constexpr (SO) {
+        // ---- the state-only pass has no C to rotate and no scores: these
+        //      warps also form W X as hi (over x) and lo (over theta, read
+        //      above) parts for MMA 4, W_j = e^{Lam_end - Lam_j} (gamma_j +
+        //      beta'_{j+1}), so that the stage's operands are ready with
+        //      the prologue
+        uint8_t* Xs = stg + Cfg::OFF_X;
+        uint8_t* WXlo = stg + Cfg::OFF_WXLO;
+#pragma unroll 1
+        for (int idx = pt; idx < MR * (P / 8); idx += NPRO) {
+          const int row = idx / (P / 8), c8 = idx % (P / 8), j = row / R;
+          const uint32_t o = sw128_offset(row, c8 * 8);
+          const uint4 raw = *reinterpret_cast<const uint4*>(Xs + o);
+          const float w = __expf(lam_end - sLam[xs][j]) * (sGam[xs][j] + sBet[j + 1]);
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = bf2_to_f2(rw[q]);
+            split_half2(w * f.x, w * f.y, hw[q], lw[q]);
+          }
+          *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
       if (pt < Q) {
         const float wp = sGam[xs][pt] + sBet[pt + 1];
         const float lt = sLam[xs][pt];
@@ -926,7 +959,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     auto state = [&](int c) -> bool {
       const int xs = c % XB;
       const bool pub = !seg_last(c);
-      bool got = wait_or_abort(saddr(&bar_scfull), (uint32_t)(c & 1), abort_flag);
+      const int sb = SO ? (c & 1) : 0;  // chunk-local state buffer
+      const uint32_t col_sc = sb ? Cfg::COL_SC1 : Cfg::COL_SC;
+      bool got = wait_or_abort(saddr(&bar_scfull[sb]), (uint32_t)((SO ? c >> 1 : c) & 1), abort_flag);
       if (!SO && got) got = wait_or_abort(saddr(&bar_rfree), (uint32_t)(c & 1), abort_flag);
       if (!group_and(2, NSTA, got)) return false;
       tc_fence_after();
@@ -936,7 +971,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       for (int hc = 0; hc < P; hc += 16) {
         float g[16], sc[16];
         tmem_ld16(tmem + lane_base + Cfg::COL_G + hc, g);
-        tmem_ld16(tmem + lane_base + Cfg::COL_SC + hc, sc);
+        tmem_ld16(tmem + lane_base + col_sc + hc, sc);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) g[i] = fmaf(elam_end, g[i], sc[i]);
@@ -955,7 +990,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       group_sync(2, NSTA);
       if (tt == 0) {
         if (!SO && pub) mbar_arrive(saddr(&bar_stready));
-        mbar_arrive(saddr(&bar_scfree));
+        mbar_arrive(saddr(&bar_scfree[sb]));
         // the state-only pass releases the chunk's scalar slot here (the
         // segment's last chunk: after finalize has read its phase)
         if (SO && pub) mbar_arrive(saddr(&bar_xfree[xs]));
@@ -1041,7 +1076,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         if (!init_seg(si)) break;
         const int end = sSegC0[si + 1];
         for (; n < end; ++n) {
-          if (!xconv(n) || (!SO && n >= 1 && !output(n - 1, ybf)) || !state(n)) {
+          if ((!SO && !xconv(n)) || (!SO && n >= 1 && !output(n - 1, ybf)) || !state(n)) {
             alive = false;
             break;
           }
@@ -1141,21 +1176,27 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           mma_commit(saddr(&bar_rfree));
           mma_commit(saddr(&bar_yfull[s]));
         }
-        // W X converted (state warps); S_{c-1} folded into the state
-        if (!wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;
-        if (c >= 1 && !wait_or_abort(saddr(&bar_scfree), (uint32_t)((c - 1) & 1), abort_flag)) break;
+        // W X converted (the state warps; SO: the prologue, with the
+        // operands); the buffer's previous chunk-local state folded into the
+        // state (S_{c-1}; SO: S_{c-2})
+        if (!SO && !wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;
+        const int sb = SO ? (c & 1) : 0;
+        const uint32_t col_sc = sb ? Cfg::COL_SC1 : Cfg::COL_SC;
+        if (SO ? (c >= 2 && !wait_or_abort(saddr(&bar_scfree[sb]), (uint32_t)(((c >> 1) - 1) & 1), abort_flag))
+               : (c >= 1 && !wait_or_abort(saddr(&bar_scfree[0]), (uint32_t)((c - 1) & 1), abort_flag)))
+          break;
         tc_fence_after();
         {  // S_c = B^T (W X) = Bhi^T WXhi + Bhi^T WXlo + Blo^T WXhi   (M = N, N = P, K = MR)
           constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
 #pragma unroll 1
           for (int ks = 0; ks < MR / 16; ++ks) {
-            mma_f16(tmem + Cfg::COL_SC, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, ks > 0);
-            mma_f16(tmem + Cfg::COL_SC, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXlo, ks, MR * 128), idesc, 1);
-            if (!RE) mma_f16(tmem + Cfg::COL_SC, mnmaj(Blo, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, 1);
+            mma_f16(tmem + col_sc, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, ks > 0);
+            mma_f16(tmem + col_sc, mnmaj(Bt, ks, Cfg::BB), mnmaj(WXlo, ks, MR * 128), idesc, 1);
+            if (!RE) mma_f16(tmem + col_sc, mnmaj(Blo, ks, Cfg::BB), mnmaj(WXt, ks, MR * 128), idesc, 1);
           }
         }
         // each commit tracks every product issued so far by this thread
-        mma_commit(saddr(&bar_scfull));
+        mma_commit(saddr(&bar_scfull[sb]));
         mma_commit(saddr(&bar_free[s]));
       }
       mma_commit(saddr(&bar_mdone[1]));
