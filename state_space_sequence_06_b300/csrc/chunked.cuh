@@ -86,24 +86,38 @@ struct ChunkParams {
   // slots leave their flags unset, so the readers' waits run out.
   unsigned long long wait_ns;
   int fault;
-  // Split schedule (split_S > 0): unit u is cut into split_S segments of
-  // split_len chunks, CTA u * split_S + s running segment s.  The
-  // state-only pass (the kernel's SO variant) runs every segment from the
-  // zero state with the carry of its previous token (handover slot
-  // blockIdx.x), writes the segment's own final state to seg_h and its total
-  // decay and rotation e^{Lam + i Phi} per pair to seg_alpha; the full pass
-  // then runs every segment from its exact initial state (slot blockIdx.x,
-  // combined from those on the device), and only the last segment of a
-  // unit writes the caller's state.
-  int split_S;
-  int split_len;
-  float* seg_h;         // [unit * split_S + s][K2][P][2]
-  float2* seg_alpha;    // [unit * split_S + s][K2]
+  // Split schedule (split_grid > 0): the units' chunks, unit after unit,
+  // are cut into split_grid equal ranges, CTA k running range k: the end of
+  // one unit and the start of the next at most (split_pieces), piece i in
+  // handover slot 2k + i.  The state-only pass (the kernel's SO variant)
+  // runs every piece that does not end its unit from the zero state with the
+  // carry of its previous token, and writes the piece's own final state to
+  // seg_h and its total decay and rotation e^{Lam + i Phi} per pair to
+  // seg_alpha; the full pass then runs every piece from its exact initial
+  // state (its slot, combined from those on the device), and only the piece
+  // that ends a unit writes the caller's state.
+  int split_grid;
+  float* seg_h;         // [slot][K2][P][2]
+  float2* seg_alpha;    // [slot][K2]
 };
 
 
 constexpr int kMaxSeg = 8;  // segments per CTA in a balanced schedule
 constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2, SEG_NO_FINAL = 4;
+
+// Split schedule: range k of `grid` equal ranges of the units' `total`
+// chunks (nch per unit, unit after unit), as at most two pieces {unit, first
+// chunk, end chunk} within their units (a range is never longer than a unit:
+// the schedule runs with grid >= units).  Returns the number of pieces.
+__host__ __device__ inline int split_pieces(int64_t nch, int64_t total, int grid, int k, int3 piece[2]) {
+  const int64_t lo = (int64_t)k * total / grid, hi = (int64_t)(k + 1) * total / grid;
+  int n = 0;
+  for (int64_t u = lo / nch; u * nch < hi && n < 2; ++u) {
+    const int64_t cb = lo > u * nch ? lo : u * nch, ce = hi < (u + 1) * nch ? hi : (u + 1) * nch;
+    if (cb < ce) piece[n++] = make_int3((int)u, (int)(cb - u * nch), (int)(ce - u * nch));
+  }
+  return n;
+}
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -155,6 +169,8 @@ struct ChunkCfg {
   static constexpr int OFF_XB = 2 * STAGE, OFF_ST = OFF_XB + XB * XT_BYTES, OFF_STLO = OFF_ST + ST_BYTES;
   static constexpr int OFF_RT = OFF_STLO + ST_BYTES;
   static constexpr int SMEM = OFF_RT + RT_BYTES + 1024;  // + alignment slack
+  // state-only pass: a stage without its C tiles (from the B tiles on)
+  static constexpr int SO_STRIDE = STAGE - OFF_B;
   static_assert(SMEM + STATIC_EST <= 232448, "shared memory of one CTA");
   // TMEM columns (f32): S[2], Y[2], Yi[2], state, chunk-local state
   static constexpr int COL_S = 0, COL_Y = 2 * MR, COL_YI = 2 * MR + 2 * P, COL_G = 2 * MR + 4 * P;
@@ -268,7 +284,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   // R).  A phase-parity wait is only sound when the waiter can never fall two
   // phases behind the barrier; each pairing below is chained so that it
   // cannot.
-  __shared__ __align__(8) uint64_t bar_full[2], bar_opready[2], bar_free[2], bar_sfull[2], bar_yfull[2];
+  // (full, opready and free per stage: NS of them)
+  __shared__ __align__(8) uint64_t bar_full[3], bar_opready[3], bar_free[3], bar_sfull[2], bar_yfull[2];
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB], bar_phend[XB];
   __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_rfree;
   // scfull / scfree per chunk-local state buffer: one buffer (index 0) in the
@@ -334,17 +351,24 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (head_seg.w >= 0) sSeg[ns++] = head_seg;
       for (int i = 0; i < nmid; ++i) sSeg[ns++] = mid[i];
       if (tail_seg.w >= 0) sSeg[ns++] = tail_seg;
-    } else if (p.split_S) {
-      // segment s of unit u; its handover slot is blockIdx.x
-      const int u = blockIdx.x / p.split_S, sgi = blockIdx.x % p.split_S;
-      const int64_t tb = (int64_t)sgi * p.split_len * Q, te0 = tb + (int64_t)p.split_len * Q;
-      const int64_t te = te0 < p.L ? te0 : p.L;
-      int fl = (int)blockIdx.x << 8;
-      if (SO)
-        fl |= SEG_SRC_SLOT | SEG_DST_SLOT;  // from the zero state and the previous token's carry
-      else
-        fl |= (sgi > 0 ? SEG_SRC_SLOT : 0) | (sgi + 1 < p.split_S ? SEG_NO_FINAL : 0);
-      if (tb < te) sSeg[ns++] = make_int4(u, (int)tb, (int)te, fl);
+    } else if (p.split_grid) {
+      // this CTA's pieces; every one starts from its handover slot (the
+      // zero state in the state-only pass, the combined state in the full
+      // pass, and the carry of the token before it in both)
+      const int64_t nch = (p.L + Q - 1) / Q;
+      int3 pc[2];
+      const int np = split_pieces(nch, (int64_t)p.bal_units * nch, p.split_grid, blockIdx.x, pc);
+      for (int i = 0; i < np; ++i) {
+        const bool ends_unit = pc[i].z == nch;
+        if (SO && ends_unit) continue;  // its own final state is needed by no later piece
+        const int tb = pc[i].y * Q, te = (int)((int64_t)pc[i].z * Q < p.L ? (int64_t)pc[i].z * Q : p.L);
+        int fl = ((2 * (int)blockIdx.x + i) << 8) | SEG_SRC_SLOT;
+        if (SO)
+          fl |= SEG_DST_SLOT;
+        else if (!ends_unit)
+          fl |= SEG_NO_FINAL;
+        sSeg[ns++] = make_int4(pc[i].x, tb, te, fl);
+      }
     } else {
       const int u = blockIdx.x, sq = u / H;
       const int n = p.cu_seqlens ? p.cu_seqlens[sq + 1] - p.cu_seqlens[sq] : (int)p.L;
@@ -382,7 +406,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   uint8_t* St = sm + Cfg::OFF_ST;
   uint8_t* Stlo = sm + Cfg::OFF_STLO;
   uint8_t* Rt = sm + Cfg::OFF_RT;
-  auto stage = [&](int s) { return sm + s * Cfg::STAGE; };
+  // Stages: two in the full pass; three in the state-only pass, whose stages
+  // hold no C tiles (stage s there starts OFF_B bytes before its B tiles,
+  // which follow the previous stage's last tile; its C offsets are unused).
+  constexpr int NS = SO ? 3 : 2;
+  static_assert(!SO || 3 * Cfg::SO_STRIDE <= Cfg::SMEM - 1024, "three state-only stages");
+  auto stage = [&](int s) { return SO ? sm + s * Cfg::SO_STRIDE - Cfg::OFF_B : sm + s * Cfg::STAGE; };
   auto xbuf = [&](int x) { return sm + Cfg::OFF_XB + x * Cfg::XT_BYTES; };
   // has the output of chunk cc (and its MMA 2) released X slot cc % XB?
   auto wait_xfree = [&](int cc) {
@@ -392,10 +421,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   if (tid == 0) {
     s_abort.flag = 0;
     s_abort.limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(saddr(&bar_full[s]), 1);
       mbar_init(saddr(&bar_opready[s]), 1);
       mbar_init(saddr(&bar_free[s]), SO ? 1 : 2);   // MMA 1 and MMAs 4/3 completions (SO: MMA 4)
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
     }
@@ -461,7 +492,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // Returns false when the pipeline was aborted.
     auto prologue = [&](int c, auto normtag) -> bool {
       constexpr bool NORM = decltype(normtag)::value;
-      const int s = c & 1, xs = c % XB;
+      const int s = c % NS, xs = c % XB;  // stage, scalar slot
       uint8_t* stg = stage(s);
       const int si = seg_of(c);
       const float A = sSegA[si];
@@ -471,7 +502,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (c == sSegC0[si] && pt < K2) sPhi[pb][pt] = 0.f;
       uint32_t d_nxt, l_nxt;
       load_scalars(c + 1, d_nxt, l_nxt, pt);
-      bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      bool got = wait_or_abort(saddr(&bar_full[s]), (uint32_t)((c / NS) & 1), abort_flag);
       // scalar slot xs last served chunk c - XB: its output must be done
       if (got && c >= XB) got = wait_xfree(c - XB);
       // Every thread waited itself.  The vote on `got` is taken at the
@@ -483,13 +514,16 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         //      as it landed; TPR adjacent threads per row, 16-byte chunks
         constexpr int TPR = NPRO / (2 * MR), CPT = N / 8 / TPR;
         const int row = pt / TPR, part = pt % TPR;
-        const bool isC = row >= MR;  // (SO: no C tile; those threads' sums are unused)
+        const bool isC = row >= MR;
         const int rr = isC ? row - MR : row;
         const uint8_t* base = stg + (isC ? Cfg::OFF_C : Cfg::OFF_B);
         const uint32_t blk_bytes = isC ? (uint32_t)(MR * 128) : (uint32_t)Cfg::BB;
         float ss = 0.f;
+        // (the state-only pass has no C tiles, and its stages no room for
+        // them: the C rows' threads read nothing, and their sums are unused)
 #pragma unroll
         for (int q = 0; q < CPT; ++q) {
+          if (SO && isC) break;
           const int col = (part * CPT + q) * 8;
           const uint4 v = *reinterpret_cast<const uint4*>(base + (col / 64) * blk_bytes + sw128_offset(rr, col % 64));
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -804,7 +838,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           return false;
         }
       }
-      const float* h0 = from_slot ? p.xh + (int64_t)slot * K2 * P * 2 : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr);
+      // (the state-only pass starts every piece from the zero state)
+      const float* h0 = SO ? nullptr
+                           : from_slot ? p.xh + (int64_t)slot * K2 * P * 2
+                                       : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr);
       const __nv_bfloat16* cB = from_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
       const __nv_bfloat16* cx = from_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
       const int64_t row0 = sSegTok0[si] * H + head;
@@ -823,10 +860,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        if (g_row >= 0 && h0) {
-          const float* hs = h0 + (int64_t)(g_row >> 1) * P * 2 + (g_row & 1);
+        if (g_row >= 0) {
+          if (h0) {
+            const float* hs = h0 + (int64_t)(g_row >> 1) * P * 2 + (g_row & 1);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2];
+            for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2];
+          }
           if (cB) {
             for (int r = 0; r < R; ++r) {
               const float b = bet0 * (norm_c ? sCarryScl[r] : 1.f) * __bfloat162float(cB[r * N + g_row]);
@@ -1152,14 +1191,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       // MMA 3 needs only this chunk's C and the R of the previous state step,
       // so it goes first; the stage is released when MMA 4 is done.
       for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        uint8_t* stg = stage(s);
+        const int s = c & 1, sg = c % NS;  // Yi buffer, stage
+        uint8_t* stg = stage(sg);
         const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
         const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
         const uint32_t WXt = saddr(stg + Cfg::OFF_X), WXlo = saddr(stg + Cfg::OFF_WXLO);
         // C of the stage rotated (prologue); R of the state at the start of chunk c
         // written; Yi[s] free (output of chunk c - 2 done)
-        if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
+        if (!wait_or_abort(saddr(&bar_opready[sg]), (uint32_t)((c / NS) & 1), abort_flag)) break;
         if (!SO) {
           if (!wait_or_abort(saddr(&bar_stready), (uint32_t)(c & 1), abort_flag)) break;
           if (c >= 2 && !wait_xfree(c - 2)) break;
@@ -1197,7 +1236,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         }
         // each commit tracks every product issued so far by this thread
         mma_commit(saddr(&bar_scfull[sb]));
-        mma_commit(saddr(&bar_free[s]));
+        mma_commit(saddr(&bar_free[sg]));
       }
       mma_commit(saddr(&bar_mdone[1]));
       mbar_wait(saddr(&bar_mdone[1]), 0, kMaxPolls);
@@ -1205,10 +1244,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   } else {
     // ======================= TMA warp (one thread issues)
     if (lane == 0) {
-      int issued0 = 0, issued1 = 0;
+      int issued[3] = {0, 0, 0};
       const int hpg = H / p.G;  // heads per B / C group
       auto issue = [&](int c) {
-        const int s = c & 1;
+        const int s = c % NS;
         uint8_t* stg = stage(s);
         const uint32_t bar = saddr(&bar_full[s]);
         const int si = seg_of(c), head = seg_head(si);
@@ -1221,9 +1260,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           if (!SO) tma_load_4d(saddr(stg + Cfg::OFF_C + kb * MR * 128), &tm_C, bar, 64 * kb, 0, head / hpg, t);
         }
         if (!RE) tma_load_3d(saddr(stg + Cfg::OFF_TH), &tm_th, bar, 0, head, t);
-        if (s) ++issued1; else ++issued0;
+        ++issued[s];
       };
-      // the stage of chunk c + 2 frees only when chunk c is done; the chunk
+      // the stage of chunk c + NS frees only when chunk c is done; the chunk
       // after it is fetched into L2 meanwhile, so its load then hits in L2
       auto prefetch = [&](int c) {
         if (c >= nchunks) return;
@@ -1241,17 +1280,16 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       tma_prefetch_desc(&tm_B);
       if (!SO) tma_prefetch_desc(&tm_C);
       if (!RE) tma_prefetch_desc(&tm_th);
-      issue(0);
-      if (nchunks > 1) issue(1);
-      prefetch(2);
-      for (int c = 0; c + 2 < nchunks; ++c) {
-        if (!wait_or_abort(saddr(&bar_free[c & 1]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
-        issue(c + 2);
-        prefetch(c + 3);
+      for (int c = 0; c < NS && c < nchunks; ++c) issue(c);
+      prefetch(NS);
+      for (int c = 0; c + NS < nchunks; ++c) {
+        if (!wait_or_abort(saddr(&bar_free[c % NS]), (uint32_t)((c / NS) & 1), abort_flag)) break;
+        issue(c + NS);
+        prefetch(c + NS + 1);
       }
       // every load issued must have landed before the CTA's shared memory goes away
-      if (issued0 > 0) mbar_wait(saddr(&bar_full[0]), (uint32_t)((issued0 - 1) & 1), kMaxPolls);
-      if (issued1 > 0) mbar_wait(saddr(&bar_full[1]), (uint32_t)((issued1 - 1) & 1), kMaxPolls);
+      for (int s = 0; s < NS; ++s)
+        if (issued[s] > 0) mbar_wait(saddr(&bar_full[s]), (uint32_t)((issued[s] - 1) & 1), kMaxPolls);
     }
   }
 
@@ -1343,46 +1381,89 @@ inline cudaMemPool_t handover_pool(int dev) {
   return pools[dev];
 }
 
-// Split schedule, before the state-only pass: handover slot u * S + s gets
-// the zero state and the carry of its segment's previous token (segment 0:
-// the caller's carry, or none), and its flag is set (nothing waits on it).
+// Split schedule, before the state-only pass: the handover slot of every
+// piece gets the carry of the token before the piece (at a unit's start:
+// the caller's carry, or none), and its flag is set (nothing waits on it);
+// its state is written by the combine.  One block per slot; slot 2k + 1 of
+// a range with one piece is unused.
 template <int N, int R, int Q>
 __global__ void __launch_bounds__(256) split_prep_kernel(const ChunkParams p) {
-  constexpr int K2 = N / 2, P = 64;
-  const int slot = blockIdx.x, u = slot / p.split_S, sgi = slot % p.split_S;
+  constexpr int P = 64;
+  const int slot = blockIdx.x;
+  const int64_t nch = (p.L + Q - 1) / Q;
+  int3 pc[2];
+  if (slot % 2 >= split_pieces(nch, (int64_t)p.bal_units * nch, p.split_grid, slot / 2, pc)) return;
+  const int u = pc[slot % 2].x, c0 = pc[slot % 2].y;
   const int head = u % p.H, b = u / p.H;
-  float* xh = p.xh + (int64_t)slot * K2 * P * 2;
-  for (int i = threadIdx.x; i < K2 * P * 2; i += blockDim.x) xh[i] = 0.f;
   const __nv_bfloat16 zero = __float2bfloat16(0.f);
   __nv_bfloat16* cB = p.xB + (int64_t)slot * R * N;
   __nv_bfloat16* cx = p.xx + (int64_t)slot * R * P;
-  const int64_t t = (int64_t)b * p.L + (int64_t)sgi * p.split_len * Q - 1;  // the previous token
+  const int64_t t = (int64_t)b * p.L + (int64_t)c0 * Q - 1;  // the previous token
   const int64_t browB = (t * p.G + head / (p.H / p.G)) * R * N, browx = (t * p.H + head) * R * P;
   for (int i = threadIdx.x; i < R * N; i += blockDim.x)
-    cB[i] = sgi > 0 ? p.B[browB + i] : (p.prev_B ? p.prev_B[(int64_t)u * R * N + i] : zero);
+    cB[i] = c0 > 0 ? p.B[browB + i] : (p.prev_B ? p.prev_B[(int64_t)u * R * N + i] : zero);
   for (int i = threadIdx.x; i < R * P; i += blockDim.x)
-    cx[i] = sgi > 0 ? p.x[browx + i] : (p.prev_x ? p.prev_x[(int64_t)u * R * P + i] : zero);
+    cx[i] = c0 > 0 ? p.x[browx + i] : (p.prev_x ? p.prev_x[(int64_t)u * R * P + i] : zero);
   if (threadIdx.x == 0) p.xflag[slot] = 1;
 }
 
-// Split schedule, between the two passes: the initial state of every
-// segment, h_in(s + 1) = alpha_s * h_in(s) + h_loc(s) with h_in(0) the
-// caller's state (zero without one), per pair and column, into the
-// segment's handover slot.  Exact: the recurrence is affine in the state,
-// and h_loc(s) already holds the segment's carry term.
-template <int N>
-__global__ void __launch_bounds__(256) split_combine_kernel(const ChunkParams p, int units) {
+// Split schedule, between the two passes: the initial state of every piece
+// of a unit, h_in(first) = the caller's state (zero without one) and
+// h_in(next) = alpha * h_in(piece) + h_loc(piece), per pair and column,
+// into the piece's handover slot.  Exact: the recurrence is affine in the
+// state, and h_loc already holds the piece's carry term.
+template <int N, int Q>
+__global__ void __launch_bounds__(256) split_combine_kernel(const ChunkParams p) {
   constexpr int K2 = N / 2, P = 64, KP = K2 * P;
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (int64_t)units * KP) return;
-  const int u = (int)(i / KP), e = (int)(i % KP), k = e / P;
+  constexpr int kMaxPieces = 256;  // pieces of one unit (the launcher keeps ranges at most 148)
+  __shared__ int sSlot[kMaxPieces];
+  __shared__ int sCount;
+  const int u = blockIdx.y;  // the unit; blockIdx.x: 256 of its K2 * P elements
+  const int64_t nch = (p.L + Q - 1) / Q, total = (int64_t)p.bal_units * nch;
+  if (threadIdx.x == 0) {  // the unit's pieces in order: the range holding its first chunk, then the next ones
+    int k = (int)(u * nch * p.split_grid / total);
+    while (k + 1 < p.split_grid && (int64_t)(k + 1) * total / p.split_grid <= u * nch) ++k;
+    while (k > 0 && (int64_t)k * total / p.split_grid > u * nch) --k;
+    int n = 0;
+    for (; k < p.split_grid && n < kMaxPieces; ++k) {
+      int3 pc[2];
+      const int np = split_pieces(nch, total, p.split_grid, k, pc);
+      int j = 0;
+      while (j < np && pc[j].x != u) ++j;
+      if (j == np) break;
+      sSlot[n++] = 2 * k + j;
+      if (pc[j].z == nch) break;  // the unit's last piece
+    }
+    sCount = n;
+  }
+  __syncthreads();
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= KP) return;
+  const int k2 = e / P;
   float2 h = p.h ? reinterpret_cast<const float2*>(p.h)[(int64_t)u * KP + e] : make_float2(0.f, 0.f);
-  for (int sgi = 0; sgi + 1 < p.split_S; ++sgi) {
-    const int64_t slot = (int64_t)u * p.split_S + sgi;
-    const float2 a = p.seg_alpha[slot * K2 + k];
-    const float2 z = reinterpret_cast<const float2*>(p.seg_h)[slot * KP + e];
-    h = make_float2(fmaf(a.x, h.x, fmaf(-a.y, h.y, z.x)), fmaf(a.x, h.y, fmaf(a.y, h.x, z.y)));
-    reinterpret_cast<float2*>(p.xh)[(slot + 1) * KP + e] = h;
+  const int n = sCount;
+  const float2* __restrict__ alpha = p.seg_alpha;
+  const float2* __restrict__ hloc = reinterpret_cast<const float2*>(p.seg_h);
+  float2* __restrict__ hin = reinterpret_cast<float2*>(p.xh);
+  // four pieces' alpha and h_loc loaded ahead of their steps (the chain
+  // through h is short arithmetic; the loads are not on it)
+  for (int i0 = 0; i0 < n; i0 += 4) {
+    float2 a[4], z[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j;
+      if (i + 1 < n) {
+        a[j] = alpha[(int64_t)sSlot[i] * K2 + k2];
+        z[j] = hloc[(int64_t)sSlot[i] * KP + e];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j;
+      if (i < n) hin[(int64_t)sSlot[i] * KP + e] = h;
+      if (i + 1 < n)
+        h = make_float2(fmaf(a[j].x, h.x, fmaf(-a[j].y, h.y, z[j].x)), fmaf(a[j].x, h.y, fmaf(a[j].y, h.x, z[j].y)));
+    }
   }
 }
 
@@ -1429,23 +1510,24 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
     return M3_ERR_CUDA;
   const int units = nseq * H;
   // Split schedule: with fewer units than SMs (one long sequence of a few
-  // heads), one CTA per unit leaves most SMs idle.  Each unit is cut into S
-  // segments instead.  A state-only pass gives every segment's own final
-  // state and total decay/rotation (all segments in parallel, no y), a small
-  // kernel chains them into each segment's exact initial state, and the full
-  // pass runs every segment from it.  At least four chunks per segment; not
-  // for packed batches or the no-allocation entry point.
+  // heads), one CTA per unit leaves most SMs idle.  The units' chunks are
+  // cut into one equal range per SM instead (a range holds the end of one
+  // unit and the start of the next at most).  A state-only pass gives every
+  // piece's own final state and total decay/rotation (all pieces in
+  // parallel, no y), a small kernel chains them into each piece's exact
+  // initial state, and the full pass runs every piece from it.  At least
+  // four chunks per range; not for packed batches or the no-allocation
+  // entry point.
   {
     int dv = 0, nsm_s = 0;
     const int64_t nch = (a->seqlen + Q - 1) / Q;
     if (!fixed && !a->cu_seqlens && a->seqlen > 0 && cudaGetDevice(&dv) == cudaSuccess &&
         cudaDeviceGetAttribute(&nsm_s, cudaDevAttrMultiProcessorCount, dv) == cudaSuccess && units < nsm_s) {
-      int S = nsm_s / units;
-      if (S > nch / 4) S = (int)(nch / 4);
-      if (S >= 2) {
-        const int len = (int)((nch + S - 1) / S);
-        S = (int)((nch + len - 1) / len);
-        const size_t nslot = (size_t)units * S;
+      const int64_t total = (int64_t)units * nch;
+      int grid = (int)(total / 4 < nsm_s ? total / 4 : nsm_s);
+      if (grid > 256) grid = 256;  // (the combine's per-unit piece list)
+      if (grid > units) {  // (so that no range is longer than a unit)
+        const size_t nslot = 2 * (size_t)grid;
         const size_t hb = nslot * (size_t)(N / 2) * 64 * 2 * 4;
         size_t off = 0;
         auto take = [&](size_t bytes) {
@@ -1462,8 +1544,8 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
         if (pool && cudaFuncSetAttribute(kso, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) == cudaSuccess &&
             cudaMallocFromPoolAsync(&buf, bytes, pool, s) == cudaSuccess) {
           uint8_t* b8 = static_cast<uint8_t*>(buf);
-          p.split_S = S;
-          p.split_len = len;
+          p.split_grid = grid;
+          p.bal_units = units;
           p.xflag = reinterpret_cast<int*>(b8 + o_flag);
           p.xh = reinterpret_cast<float*>(b8 + o_xh);
           p.xB = reinterpret_cast<__nv_bfloat16*>(b8 + o_xB);
@@ -1471,13 +1553,12 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
           p.seg_h = reinterpret_cast<float*>(b8 + o_sh);
           p.seg_alpha = reinterpret_cast<float2*>(b8 + o_sa);
           split_prep_kernel<N, R, Q><<<(unsigned)nslot, 256, 0, s>>>(p);
-          kso<<<(unsigned)nslot, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
-          const int64_t nel = (int64_t)units * (N / 2) * 64;
-          split_combine_kernel<N><<<(unsigned)((nel + 255) / 256), 256, 0, s>>>(p, units);
-          kern<<<(unsigned)nslot, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+          kso<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+          split_combine_kernel<N, Q><<<dim3((N / 2) * 64 / 256, (unsigned)units), 256, 0, s>>>(p);
+          kern<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
           const cudaError_t e = cudaGetLastError();
           const cudaError_t ef = cudaFreeAsync(buf, s);
-          record_launch(M3_TEST_KERNEL_CHUNKED_SPLIT, (int)nslot, (long long)bytes);
+          record_launch(M3_TEST_KERNEL_CHUNKED_SPLIT, grid, (long long)bytes);
           return (e == cudaSuccess && ef == cudaSuccess) ? M3_OK : M3_ERR_CUDA;
         }
         cudaGetLastError();  // no pool memory: the one-CTA-per-unit launch below
