@@ -737,13 +737,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const int cl = 2 * (lane % 4);        // this thread's column pair inside each 8-column group
 #pragma unroll 1
       for (int cb = 0; cb < CPH; cb += 16) {
+        if ((cbeg + cb) / R > it_warp) break;  // this and later column blocks: all masked, zeros in place
         float sv[8];  // [group gg][4]: (r0, c), (r0, c+1), (r0+8, c), (r0+8, c+1)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sv[i] = 0.f;
-        if ((cbeg + cb) / R <= it_warp) {
-          tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, sv);
-          tmem_ld_wait();
-        }
+        tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, sv);
+        tmem_ld_wait();
 #pragma unroll
         for (int gg = 0; gg < 2; ++gg) {
           const int j = cbeg + cb + 8 * gg + cl;  // first of this thread's two columns
@@ -789,6 +786,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // compiled once with and once without the BC norm (the real-state
     // variant has none: its B and C reach the MMAs without a lo part)
     auto run = [&](auto normtag) {
+      // S' blocks above the diagonal are zero in every chunk: written once
+      // here and skipped by S -> S' (ordered before MMA 2 by the first
+      // S -> S' barrier)
+      if (!SO) {
+        for (int i = pt; i < 2 * Cfg::ST_BYTES / 16; i += NPRO)
+          reinterpret_cast<uint4*>(St)[i] = make_uint4(0u, 0u, 0u, 0u);  // (Stlo follows St)
+        fence_async_smem();
+      }
       bool alive = prologue(0, normtag);
       for (int c = 0; c < nchunks && alive; ++c) {
         if (c + 1 < nchunks && !prologue(c + 1, normtag)) break;
