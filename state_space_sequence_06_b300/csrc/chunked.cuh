@@ -57,6 +57,9 @@ struct ChunkParams {
   const float* A;
   const float* D;
   const int32_t* cu_seqlens;  // NULL: fixed length L per batch row
+  // one CTA per unit with packed sequences: CTA b runs head b % H of
+  // sequence seq_order[b / H] (longest sequences first), or unit b when NULL
+  const int32_t* seq_order;
   void* y;                  // f32, or bf16 when ybf
   int ybf;
   float* h;                 // state slots or NULL
@@ -370,7 +373,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         sSeg[ns++] = make_int4(pc[i].x, tb, te, fl);
       }
     } else {
-      const int u = blockIdx.x, sq = u / H;
+      const int u = p.seq_order ? p.seq_order[blockIdx.x / H] * H + (int)blockIdx.x % H : (int)blockIdx.x;
+      const int sq = u / H;
       const int n = p.cu_seqlens ? p.cu_seqlens[sq + 1] - p.cu_seqlens[sq] : (int)p.L;
       if (n > 0) sSeg[ns++] = make_int4(u, 0, n, 0);
     }
@@ -1472,6 +1476,23 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const ChunkParams p)
   }
 }
 
+// Packed sequences, one CTA per unit: the sequences by length, longest
+// first (ties by index), so that the block scheduler starts the longest
+// units first and the short ones fill in behind them (longest processing
+// time first).  One block; nseq <= kMaxOrderSeq.
+constexpr int kMaxOrderSeq = 2048;
+__global__ void __launch_bounds__(1024) seq_order_kernel(const int32_t* cu, int nseq, int32_t* order) {
+  __shared__ int len[kMaxOrderSeq];
+  for (int i = threadIdx.x; i < nseq; i += blockDim.x) len[i] = cu[i + 1] - cu[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
+    const int li = len[i];
+    int rank = 0;
+    for (int j = 0; j < nseq; ++j) rank += (len[j] > li) | ((len[j] == li) & (j < i));
+    order[rank] = i;
+  }
+}
+
 // fixed: caller-provided scratch (fixed_bytes long) for the handover slots
 // instead of the pool; a request that needs more is refused.
 template <int N, int R, int Q, bool RE>
@@ -1614,6 +1635,27 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
       }
       cudaGetLastError();  // no pool memory: the one-CTA-per-unit launch below
     }
+  }
+  // packed sequences of different lengths on more units than SMs: the
+  // longest units first (the order comes from the pool; without pool
+  // memory, or with the caller's fixed scratch, the natural order)
+  if (a->cu_seqlens && !fixed && nseq >= 2 && nseq <= kMaxOrderSeq) {
+    int dv = 0, nsm_o = 0;
+    void* buf = nullptr;
+    cudaMemPool_t pool = nullptr;
+    if (cudaGetDevice(&dv) == cudaSuccess &&
+        cudaDeviceGetAttribute(&nsm_o, cudaDevAttrMultiProcessorCount, dv) == cudaSuccess && units > nsm_o &&
+        (pool = handover_pool(dv)) != nullptr &&
+        cudaMallocFromPoolAsync(&buf, (size_t)nseq * sizeof(int32_t), pool, s) == cudaSuccess) {
+      p.seq_order = static_cast<const int32_t*>(buf);
+      seq_order_kernel<<<1, 1024, 0, s>>>(a->cu_seqlens, nseq, static_cast<int32_t*>(buf));
+      kern<<<units, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+      const cudaError_t e = cudaGetLastError();
+      const cudaError_t ef = cudaFreeAsync(buf, s);
+      record_launch(M3_TEST_KERNEL_CHUNKED, units, (long long)((size_t)nseq * sizeof(int32_t)));
+      return (e == cudaSuccess && ef == cudaSuccess) ? M3_OK : M3_ERR_CUDA;
+    }
+    cudaGetLastError();
   }
   kern<<<units, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
   record_launch(M3_TEST_KERNEL_CHUNKED, units, 0);

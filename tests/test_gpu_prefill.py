@@ -158,6 +158,34 @@ def test_varlen_small(algo):
     st.free()
 
 
+def test_varlen_more_units_than_sms_longest_first():
+    """More (sequence, head) units than SMs in a packed batch: the chunked
+    launch runs the longest sequences' units first (an order computed on
+    the device, ties and empty sequences included); every output, final
+    state and carry against the oracle."""
+    lens = [130, 0, 64, 257, 1, 130, 65, 200, 33, 0, 129, 64]
+    cu = synth.varlen_cu_seqlens(lens)
+    wl = synth.scaled(synth.workloads()["varlen_16"], seqlen=int(cu[-1]), nheads=16, nseq=len(lens),
+                      cu_seqlens=cu, h0_std=0.2, carry=True)
+    wl_state = synth.scaled(wl, batch=len(lens))
+    inp = synth.prefill_inputs(wl)
+    init = synth.prefill_inputs(wl_state)
+    st = state_for(dims_of(wl, batch=len(lens)), init["h0"], init["prev_B"], init["prev_x"])
+    y = prefill_gpu(inp, wl, state=st, cu=cu, algo=0)
+    info = m3.m3_test_last_launch()
+    y = y.cpu().numpy()
+    assert info.kernel == m3.M3_TEST_KERNEL_CHUNKED and info.grid == 16 * len(lens)
+    assert info.scratch_bytes == 4 * len(lens)  # the sequence order
+    yo, ho, pBo, pxo, _ = oracle.prefill(inp, **oracle_kw(wl), cu_seqlens=cu, h0=init["h0"],
+                                         prev_B=init["prev_B"], prev_x=init["prev_x"])
+    assert_close(y, yo, TOL["bf16"], "varlen y")
+    h, pB, px = st.views()
+    assert_close(to_np(h).reshape(ho.shape), ho, TOL["bf16"], "varlen h")
+    assert np.array_equal(to_np(pB).reshape(pBo.shape), pBo)
+    assert np.array_equal(to_np(px).reshape(pxo.shape), pxo)
+    st.free()
+
+
 def test_empty_sequence_is_noop():
     wl = synth.scaled(synth.workloads()["siso_b8_l4096"], batch=1, seqlen=0, nheads=1)
     x = torch.empty((1, 0, 1, 1, 64), dtype=torch.bfloat16, device="cuda")
