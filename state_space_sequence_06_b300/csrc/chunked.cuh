@@ -869,12 +869,35 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        if (g_row >= 0) {
-          if (h0) {
-            const float* hs = h0 + (int64_t)(g_row >> 1) * P * 2 + (g_row & 1);
+        if (h0) {
+          // the 16 columns of pair g_row / 2 are 128 contiguous bytes (re, im
+          // interleaved): the re lane loads columns cb..cb+7, the im lane
+          // cb+8..cb+15, and each passes the other the half it needs
+          const bool re = (g_row & 1) == 0;
+          float own[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = hs[(cb + i) * 2];
+          for (int i = 0; i < 16; ++i) own[i] = 0.f;
+          if (g_row >= 0) {
+            const float4* hs = reinterpret_cast<const float4*>(h0 + (int64_t)(g_row >> 1) * P * 2 + (cb + (re ? 0 : 8)) * 2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 f = hs[q];
+              own[4 * q] = f.x;
+              own[4 * q + 1] = f.y;
+              own[4 * q + 2] = f.z;
+              own[4 * q + 3] = f.w;
+            }
           }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            // (selects, not lane-dependent indices, keep the arrays in registers)
+            const float mine = re ? own[2 * i] : own[2 * i + 1];  // this lane's part of its own columns
+            const float other = __shfl_xor_sync(0xffffffffu, re ? own[2 * i + 1] : own[2 * i], 1);
+            v[i] = re ? mine : other;
+            v[8 + i] = re ? other : mine;
+          }
+        }
+        if (g_row >= 0) {
           if (cB) {
             for (int r = 0; r < R; ++r) {
               const float b = bet0 * (norm_c ? sCarryScl[r] : 1.f) * __bfloat162float(cB[r * N + g_row]);
@@ -898,6 +921,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       tc_fence_before();
       group_sync(2, NSTA);
       if (!SO && tt == 0) mbar_arrive(saddr(&bar_stready));
+      // the next segment's initial state, when it is the caller's: into L2
+      // now, so that its loads hit there when that segment starts
+      if (si + 1 < nseg && !(sSeg[si + 1].w & SEG_SRC_SLOT) && p.h) {
+        const char* nh = reinterpret_cast<const char*>(p.h + (int64_t)sSeg[si + 1].x * K2 * P * 2);
+        for (int off = tt * 128; off < K2 * P * 2 * 4; off += NSTA * 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(nh + off));
+      }
       return true;
     };
     // final state of segment si (h of its last token, rotated back by the
@@ -938,10 +968,19 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
             v[i] = re ? (cs * v[i] - sn * other) : (sn * other + cs * v[i]);
           }
-          if (g_row >= 0) {
-            float* hs = hd + (int64_t)(g_row >> 1) * P * 2 + (g_row & 1);
+          // (re, im) of columns cb..cb+7 from the re lane, cb+8..cb+15 from
+          // the im lane: 64 contiguous bytes each
+          float out[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) hs[(cb + i) * 2] = v[i];
+          for (int i = 0; i < 8; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, re ? v[8 + i] : v[i], 1);
+            out[2 * i] = re ? v[i] : other;
+            out[2 * i + 1] = re ? other : v[8 + i];
+          }
+          if (g_row >= 0) {
+            float4* hs = reinterpret_cast<float4*>(hd + (int64_t)(g_row >> 1) * P * 2 + (cb + (re ? 0 : 8)) * 2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hs[q] = make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
           }
         }
       }
