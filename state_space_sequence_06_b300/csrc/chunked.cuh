@@ -106,7 +106,12 @@ struct ChunkParams {
 
 
 constexpr int kMaxSeg = 8;  // segments per CTA in a balanced schedule
-constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2, SEG_NO_FINAL = 4;
+// SEG_SPLIT: a piece of the split schedule: its carry is the previous
+// token's own B and x rows (at a unit's start the caller's carry, which
+// the full pass reads from a copy in the piece's slot: the unit's last
+// piece overwrites the caller's), and its slot is ready when the kernel
+// starts (no flag to wait for)
+constexpr int SEG_SRC_SLOT = 1, SEG_DST_SLOT = 2, SEG_NO_FINAL = 4, SEG_SPLIT = 8;
 
 // Split schedule: range k of `grid` equal ranges of the units' `total`
 // chunks (nch per unit, unit after unit), as at most two pieces {unit, first
@@ -355,9 +360,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       for (int i = 0; i < nmid; ++i) sSeg[ns++] = mid[i];
       if (tail_seg.w >= 0) sSeg[ns++] = tail_seg;
     } else if (p.split_grid) {
-      // this CTA's pieces; every one starts from its handover slot (the
-      // zero state in the state-only pass, the combined state in the full
-      // pass, and the carry of the token before it in both)
+      // this CTA's pieces; every one starts from the zero state in the
+      // state-only pass and from its handover slot (the combined state) in
+      // the full pass, with the carry of the token before it in both
       const int64_t nch = (p.L + Q - 1) / Q;
       int3 pc[2];
       const int np = split_pieces(nch, (int64_t)p.bal_units * nch, p.split_grid, blockIdx.x, pc);
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         const bool ends_unit = pc[i].z == nch;
         if (SO && ends_unit) continue;  // its own final state is needed by no later piece
         const int tb = pc[i].y * Q, te = (int)((int64_t)pc[i].z * Q < p.L ? (int64_t)pc[i].z * Q : p.L);
-        int fl = ((2 * (int)blockIdx.x + i) << 8) | SEG_SRC_SLOT;
+        int fl = ((2 * (int)blockIdx.x + i) << 8) | SEG_SRC_SLOT | SEG_SPLIT;
         if (SO)
           fl |= SEG_DST_SLOT;
         else if (!ends_unit)
@@ -826,8 +831,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       seg_decay = 1.f;
       const int unit = sg.x, head = unit % H;
       const bool from_slot = (sg.w & SEG_SRC_SLOT) != 0;
+      const bool split = (sg.w & SEG_SPLIT) != 0;
       const int slot = sg.w >> 8;
-      if (from_slot) {  // bounded wait for the CTA that runs the first part of this unit
+      if (from_slot && !split) {  // bounded wait for the CTA that runs the first part of this unit
         bool ok = false;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t i = 0; i < kMaxPolls; ++i) {
@@ -853,6 +859,16 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
                                        : (p.h ? p.h + (int64_t)unit * K2 * P * 2 : nullptr);
       const __nv_bfloat16* cB = from_slot ? p.xB + (int64_t)slot * R * N : (p.prev_B ? p.prev_B + (int64_t)unit * R * N : nullptr);
       const __nv_bfloat16* cx = from_slot ? p.xx + (int64_t)slot * R * P : (p.prev_x ? p.prev_x + (int64_t)unit * R * P : nullptr);
+      if (split) {  // the previous token's rows, or the caller's carry at the unit's start
+        const int64_t tp = sSegTok0[si] - 1;
+        if (sg.y > 0) {
+          cB = p.B + (tp * p.G + head / (H / p.G)) * R * N;
+          cx = p.x + (tp * H + head) * R * P;
+        } else {
+          cB = p.prev_B ? (SO ? p.prev_B + (int64_t)unit * R * N : p.xB + (int64_t)slot * R * N) : nullptr;
+          cx = p.prev_x ? (SO ? p.prev_x + (int64_t)unit * R * P : p.xx + (int64_t)slot * R * P) : nullptr;
+        }
+      }
       const int64_t row0 = sSegTok0[si] * H + head;
       const float dt0 = scan_dt(__bfloat162float(p.dt[row0]), p.pro, p.dt_bias, head);
       const float lm0 = p.lam ? __bfloat162float(p.lam[row0]) : 1.f;
@@ -1429,38 +1445,14 @@ inline cudaMemPool_t handover_pool(int dev) {
   return pools[dev];
 }
 
-// Split schedule, before the state-only pass: the handover slot of every
-// piece gets the carry of the token before the piece (at a unit's start:
-// the caller's carry, or none), and its flag is set (nothing waits on it);
-// its state is written by the combine.  One block per slot; slot 2k + 1 of
-// a range with one piece is unused.
-template <int N, int R, int Q>
-__global__ void __launch_bounds__(256) split_prep_kernel(const ChunkParams p) {
-  constexpr int P = 64;
-  const int slot = blockIdx.x;
-  const int64_t nch = (p.L + Q - 1) / Q;
-  int3 pc[2];
-  if (slot % 2 >= split_pieces(nch, (int64_t)p.bal_units * nch, p.split_grid, slot / 2, pc)) return;
-  const int u = pc[slot % 2].x, c0 = pc[slot % 2].y;
-  const int head = u % p.H, b = u / p.H;
-  const __nv_bfloat16 zero = __float2bfloat16(0.f);
-  __nv_bfloat16* cB = p.xB + (int64_t)slot * R * N;
-  __nv_bfloat16* cx = p.xx + (int64_t)slot * R * P;
-  const int64_t t = (int64_t)b * p.L + (int64_t)c0 * Q - 1;  // the previous token
-  const int64_t browB = (t * p.G + head / (p.H / p.G)) * R * N, browx = (t * p.H + head) * R * P;
-  for (int i = threadIdx.x; i < R * N; i += blockDim.x)
-    cB[i] = c0 > 0 ? p.B[browB + i] : (p.prev_B ? p.prev_B[(int64_t)u * R * N + i] : zero);
-  for (int i = threadIdx.x; i < R * P; i += blockDim.x)
-    cx[i] = c0 > 0 ? p.x[browx + i] : (p.prev_x ? p.prev_x[(int64_t)u * R * P + i] : zero);
-  if (threadIdx.x == 0) p.xflag[slot] = 1;
-}
-
 // Split schedule, between the two passes: the initial state of every piece
 // of a unit, h_in(first) = the caller's state (zero without one) and
 // h_in(next) = alpha * h_in(piece) + h_loc(piece), per pair and column,
 // into the piece's handover slot.  Exact: the recurrence is affine in the
-// state, and h_loc already holds the piece's carry term.
-template <int N, int Q>
+// state, and h_loc already holds the piece's carry term.  Block 0 of a
+// unit also copies the caller's carry into the slot of the unit's first
+// piece (the full pass overwrites the caller's with the unit's last token).
+template <int N, int R, int Q>
 __global__ void __launch_bounds__(256) split_combine_kernel(const ChunkParams p) {
   constexpr int K2 = N / 2, P = 64, KP = K2 * P;
   constexpr int kMaxPieces = 256;  // pieces of one unit (the launcher keeps ranges at most 148)
@@ -1485,6 +1477,13 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const ChunkParams p)
     sCount = n;
   }
   __syncthreads();
+  if (blockIdx.x == 0 && sCount > 0) {  // the caller's carry, for the full pass of the unit's first piece
+    const int64_t s0 = sSlot[0];
+    if (p.prev_B)
+      for (int i = threadIdx.x; i < R * N; i += blockDim.x) p.xB[s0 * R * N + i] = p.prev_B[(int64_t)u * R * N + i];
+    if (p.prev_x)
+      for (int i = threadIdx.x; i < R * P; i += blockDim.x) p.xx[s0 * R * P + i] = p.prev_x[(int64_t)u * R * P + i];
+  }
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= KP) return;
   const int k2 = e / P;
@@ -1580,7 +1579,8 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   // unit and the start of the next at most).  A state-only pass gives every
   // piece's own final state and total decay/rotation (all pieces in
   // parallel, no y), a small kernel chains them into each piece's exact
-  // initial state, and the full pass runs every piece from it.  At least
+  // initial state (and copies the caller's carry for each unit's first
+  // piece), and the full pass runs every piece from it.  At least
   // four chunks per range; not for packed batches or the no-allocation
   // entry point.
   {
@@ -1600,8 +1600,8 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
           off += (bytes + 255) / 256 * 256;
           return o;
         };
-        const size_t o_flag = take(nslot * 4), o_xh = take(hb), o_xB = take(nslot * R * N * 2),
-                     o_xx = take(nslot * R * 64 * 2), o_sh = take(hb), o_sa = take(nslot * (N / 2) * 8);
+        const size_t o_xh = take(hb), o_sh = take(hb), o_sa = take(nslot * (N / 2) * 8),
+                     o_xB = take(nslot * R * N * 2), o_xx = take(nslot * R * 64 * 2);
         const size_t bytes = off;
         cudaMemPool_t pool = handover_pool(dv);
         void* buf = nullptr;
@@ -1611,15 +1611,13 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
           uint8_t* b8 = static_cast<uint8_t*>(buf);
           p.split_grid = grid;
           p.bal_units = units;
-          p.xflag = reinterpret_cast<int*>(b8 + o_flag);
           p.xh = reinterpret_cast<float*>(b8 + o_xh);
           p.xB = reinterpret_cast<__nv_bfloat16*>(b8 + o_xB);
           p.xx = reinterpret_cast<__nv_bfloat16*>(b8 + o_xx);
           p.seg_h = reinterpret_cast<float*>(b8 + o_sh);
           p.seg_alpha = reinterpret_cast<float2*>(b8 + o_sa);
-          split_prep_kernel<N, R, Q><<<(unsigned)nslot, 256, 0, s>>>(p);
           kso<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
-          split_combine_kernel<N, Q><<<dim3((N / 2) * 64 / 256, (unsigned)units), 256, 0, s>>>(p);
+          split_combine_kernel<N, R, Q><<<dim3((N / 2) * 64 / 256, (unsigned)units), 256, 0, s>>>(p);
           kern<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
           const cudaError_t e = cudaGetLastError();
           const cudaError_t ef = cudaFreeAsync(buf, s);
