@@ -60,8 +60,10 @@ struct DecodeParams {
 // float4 per pair) read with 128-bit broadcast loads (every lane of a warp
 // works on the same k); each thread keeps the x values of its two p columns
 // in registers.
+// (rank 4 runs 128-thread CTAs: nine of them resident per SM, their
+// registers and shared memory sized for it)
 template <typename T, int ITEMS, int R_, bool YB>
-__global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(R_ == 4 ? 128 : 256, R_ == 4 ? 9 : 0) decode_step_kernel(const DecodeParams p) {
   using namespace umma;
   extern __shared__ float4 smem4[];
   __shared__ __align__(8) uint64_t bar;
@@ -69,12 +71,18 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
   constexpr int KW = (3 * RMAX + 2) / 2;  // float4 per pair record
   const int R = R_ > 0 ? R_ : p.R;
   const int K = p.K, N = p.N, P = p.P, PP = p.PP, KG = p.KG;
-  float4* hsm = smem4;                                         // [K][PP]: the state, (re, im) x 2 per float4
-  float4* kd = hsm + (size_t)K * PP;                           // [K][KW]
-  float* xs = reinterpret_cast<float*>(kd + (size_t)K * KW);   // [2][R][P]: this token's x, previous x
-  float* red = xs + 2 * R * P;                                 // [KG][R][P]
+  float4* hsm = smem4;                                          // [K][PP]: the state, (re, im) x 2 per float4
+  float* xs = reinterpret_cast<float*>(hsm + (size_t)K * PP);   // [2][R][P]: this token's x, previous x
+  float4* kd = reinterpret_cast<float4*>(xs + 2 * RMAX * P);   // [K][KW] (16-byte aligned: RMAX * P is even)
   // raw per-unit inputs, when they arrive by bulk copy: B, C, prev B [R][N], x, prev x [R][P], theta [K]
-  T* rawB = reinterpret_cast<T*>((reinterpret_cast<uintptr_t>(red + KG * R * P) + 15) & ~uintptr_t(15));
+  T* rawB = reinterpret_cast<T*>(kd + (size_t)K * KW);
+  // the partial outputs [KG][R][P]: after the raw inputs for rank 1; for
+  // higher ranks (larger records and outputs) in the records' and raw
+  // inputs' room, once the update is done with them
+  constexpr bool kRedOverRecords = R_ != 1;
+  const T* raw_end = rawB + (p.bulk ? 3 * R * N + 2 * R * P + K : 0);
+  float* red = kRedOverRecords ? reinterpret_cast<float*>(kd)
+                               : reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(raw_end) + 15) & ~uintptr_t(15));
   T* rawC = rawB + R * N;
   T* rawPB = rawC + R * N;
   T* rawX = rawPB + R * N;
@@ -233,7 +241,13 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecodeParams p) 
     }
   }
 
-  // 5. write the state back (one bulk copy) and reduce the partial outputs.
+  // 5. write the state back (one bulk copy) and reduce the partial outputs
+  //    (over the records and raw inputs: every thread is past the update,
+  //    and the carry's copy has read its rows)
+  if (kRedOverRecords) {
+    if (tid == 0 && p.bulk) bulk_wait_read_all();
+    __syncthreads();
+  }
 #pragma unroll
   for (int r = 0; r < RMAX; ++r) {
     if (r >= R) break;

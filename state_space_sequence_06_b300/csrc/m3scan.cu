@@ -105,8 +105,12 @@ m3_status decode_launch(m3::DecodeParams p, int units, cudaStream_t s) {
             al16(p.x) && al16(p.B) && al16(p.C) && al16(p.theta) && al16(p.prev_B) && al16(p.prev_x))
                ? 1
                : 0;
-  const size_t smem = sizeof(float4) * p.K * (p.PP + kw) + sizeof(float) * (2 * p.R * p.P + kg * p.R * p.P) +
-                      (p.bulk ? raw + 16 : 0);
+  // (layout: state, x rows, the records and raw inputs, then the partial
+  // outputs -- which, above rank 1, reuse the records' and raw inputs' room)
+  const size_t tail = sizeof(float4) * p.K * kw + (p.bulk ? raw : 0);
+  const size_t red = sizeof(float) * (size_t)kg * p.R * p.P;
+  const size_t smem = sizeof(float4) * p.K * p.PP + sizeof(float) * 2 * rmax * p.P +
+                      (p.R == 1 ? tail + 16 + red : (tail > red ? tail : red));
   if (smem > 200 * 1024) return M3_ERR_UNSUPPORTED;
   return p.ybf ? decode_items<T, true>(p, items, threads, smem, units, s)
                : decode_items<T, false>(p, items, threads, smem, units, s);
