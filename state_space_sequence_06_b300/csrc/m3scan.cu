@@ -86,8 +86,10 @@ m3_status decode_launch(m3::DecodeParams p, int units, cudaStream_t s) {
   p.PP = p.P / 2;
   if (p.PP > 256) return M3_ERR_UNSUPPORTED;
   // rank > 1 keeps more per-thread registers (x columns and outputs per
-  // rank): smaller CTAs keep more of them resident per SM
-  int kg = (p.R == 1 ? 256 : 128) / p.PP;
+  // rank), and a 16 KB state (N 64) leaves room for more CTAs than
+  // 256-thread ones' registers allow: smaller CTAs keep more of them
+  // resident per SM
+  int kg = (p.R == 1 && p.N > 64 ? 256 : 128) / p.PP;
   if (kg < 1) kg = 1;
   while (ceil_div(p.K, kg) > 16 && p.PP * kg * 2 <= 256) kg *= 2;
   if (kg > p.K) kg = p.K;
