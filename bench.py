@@ -643,8 +643,9 @@ def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
     dL/dy and dL/dh_final; one pass = every gradient of the batch (the
     chunked kernels where the shape has them: --algo auto or chunked; the
     token-serial kernel: --algo recurrent).  Roofline: the contraction
-    FLOPs of the chunked form against the FP32 FMA peak (the kernels are
-    f32 SIMT: bound "alu").  Unit 0's gradients are checked against the
+    FLOPs of the chunked form against the FP32 FMA peak (the dominant
+    kernel, the chunk gradients, is f32 SIMT: bound "alu"; the chunk sums
+    run on the tensor cores for ranks 1 and 2).  Unit 0's gradients are checked against the
     oracle's adjoint."""
     import oracle
 
@@ -699,7 +700,8 @@ def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
     alu_peak = fp32_peak_tflops()
     achieved = flops / (per_ms / 1e3) / 1e12
     if rank == 0:
-        kernel = "token-serial" if algo == m3.M3_ALGO_RECURRENT else "chunked (f32 SIMT)"
+        kernel = ("token-serial" if algo == m3.M3_ALGO_RECURRENT
+                  else "chunked (f32 SIMT gradients; tcgen05 chunk sums for ranks 1 and 2)")
         print(json.dumps({
             "metric": "Mamba-3 scan backward tokens/s", "value": b * L * world / (per_ms / 1e3), "unit": "tokens/s",
             "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": per_ms,

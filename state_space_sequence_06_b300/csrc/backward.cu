@@ -7,6 +7,10 @@
 #include "bwd_chunked.cuh"
 #include "m3scan_backward.h"
 
+namespace m3 {
+int* device_status_word();  // (m3scan.cu)
+}
+
 namespace m3bwd {
 
 // ------------------------------------------------------------------ prologue passes
@@ -185,9 +189,14 @@ m3_status chunked_go(const m3_backward_args* a, const void* const in[8], int G, 
   take(9, bc_head);                               // per-head dB
   take(10, bc_head);                              // per-head dC
   if (tot > (size_t(16) << 30)) return M3_ERR_UNSUPPORTED;
-  const size_t smem1 = sizeof(float) * (2 * MR * NS + 2 * MR * PS);  // (the angles share the dy tile)
+  // chunk sums on the tensor cores; with rank 4 (16-token chunks, four
+  // times as many) the f32 kernel, whose fixed cost per chunk is lower
+  // (TMEM allocation, the MMA round trip), measured faster
+  constexpr bool kSumsTc = RR < 4;
+  const size_t smem1 = kSumsTc ? (size_t)SumsTcLayout<NN, MR>::SMEM
+                               : sizeof(float) * (2 * MR * NS + 2 * MR * PS);  // (the angles share the dy tile)
   const size_t smem3 = sizeof(float) * (2 * MR * NS + 2 * MR * PS + 2 * NN * PS + 2 * MR * MS + Q * K);
-  auto k1 = chunk_sums_kernel<T, NN, RR>;
+  auto k1 = kSumsTc ? chunk_sums_tc_kernel<T, NN, RR> : chunk_sums_kernel<T, NN, RR>;
   auto k3 = chunk_grads_kernel<T, NN, RR>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess ||
       cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3) != cudaSuccess)
@@ -217,6 +226,11 @@ m3_status chunked_go(const m3_backward_args* a, const void* const in[8], int G, 
   p.dA_part = static_cast<float*>(at(7));
   p.dD_part = static_cast<float*>(at(8));
   p.L = L; p.nch = nch; p.H = H; p.G = G; p.GB = H;
+  p.status = m3::device_status_word();
+  if (!p.status) {
+    cudaFreeAsync(buf, s);
+    return M3_ERR_CUDA;
+  }
   const unsigned chunks = (unsigned)(units * nch);
   k1<<<chunks, Cfg::NT, smem1, s>>>(p);
   const unsigned bpu = (unsigned)((KP + 255) / 256);

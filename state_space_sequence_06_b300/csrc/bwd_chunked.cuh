@@ -41,8 +41,13 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
+
+#include "umma.cuh"
 
 namespace m3bwd {
 
@@ -82,6 +87,7 @@ struct ChunkBwdParams {
   int64_t L;
   int nch;
   int H, G, GB;  // heads, B/C groups of the inputs, rows of the dB/dC written here
+  int* status;   // the library's device status word (a bounded wait that gives up writes M3_ERR_TIMEOUT)
 };
 
 template <typename T>
@@ -375,6 +381,210 @@ __global__ void __launch_bounds__(256) chunk_sums_kernel(const ChunkBwdParams p)
     const float e = expf(s.Lam[n - 1]);
     p.alpha[(int64_t)unit * p.nch * K + (int64_t)c * K + k] = make_float2(e * cs, e * sn);
   }
+}
+
+// Phase 1 on the tensor cores: the same two products per chunk, Z = Bt^T
+// (f x) and U = Ct^T (e^{Lam} dy) (N x P each, K = MR rows), as tcgen05
+// MMAs from 128-byte-swizzled f16 tiles into TMEM.  Every operand is an
+// f16 hi + lo pair (hi·hi + hi·lo + lo·hi, about 21 bits, as in the
+// forward kernel); the rotated rows are the MN-major A operand (M = N state
+// rows), x and dy the MN-major B operand (N = P).  Tiles: the rotated B
+// and C rows [N/64 blocks][MR rows][128 B], hi and lo apart; x and dy rows
+// [MR rows][128 B]; the local angles share the dy tiles until dy is
+// loaded.  One thread issues the MMAs; every thread waits (bounded) on
+// their commit, then warp w reads accumulator rows of TMEM lane quarter
+// w % 4, Z for w < 4 and U for w >= 4.
+__device__ __forceinline__ void half2_hilo(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+template <int N, int MR>
+struct SumsTcLayout {
+  static constexpr int P = 64;
+  static constexpr int BT = N * MR * 2;  // one f16 tile of rotated rows
+  static constexpr int XT = MR * P * 2;  // one f16 tile of x or dy rows
+  static constexpr int OFF_BHI = 0, OFF_BLO = BT, OFF_CHI = 2 * BT, OFF_CLO = 3 * BT;
+  static constexpr int OFF_XHI = 4 * BT, OFF_XLO = OFF_XHI + XT, OFF_YHI = OFF_XLO + XT, OFF_YLO = OFF_YHI + XT;
+  static constexpr int SMEM = OFF_YLO + XT + 1024;  // + alignment of the tiles to 1024 B
+  static constexpr int TCOLS = 2 * P;               // Z, then U
+};
+
+constexpr uint32_t kSumsMaxPolls = 1u << 26;  // far beyond the few microseconds the products take
+
+template <typename T, int N_, int R_>
+__global__ void __launch_bounds__(256, 2) chunk_sums_tc_kernel(const ChunkBwdParams p) {
+  using namespace m3::umma;
+  using Cfg = BwdCfg<N_, R_>;
+  using Lay = SumsTcLayout<N_, Cfg::MR>;
+  constexpr int N = Cfg::N, R = Cfg::R, P = Cfg::P, MR = Cfg::MR, Q = Cfg::Q, K = Cfg::K, NT = Cfg::NT;
+  static_assert(NT == 256, "eight warps: four lane quarters for each of Z and U");
+  static_assert(Q * K * 4 <= 2 * Lay::XT, "the angles fit in the dy tiles");
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = smraw + ((1024u - (saddr(smraw) & 1023u)) & 1023u);
+  float* phi = reinterpret_cast<float*>(sm + Lay::OFF_YHI);  // [Q][K] angles, until dy is loaded
+  __shared__ ChunkScalars<Q> s;
+  __shared__ float sred[32];
+  __shared__ float sPhiEnd[K];
+  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ uint32_t tmem_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x % p.nch, unit = blockIdx.x / p.nch;
+  const int b = unit / p.H, head = unit % p.H, grp = head / (p.H / p.G);
+  const int64_t tok0 = (int64_t)b * p.L + (int64_t)c * Q;
+  const int n = (int)((p.L - (int64_t)c * Q) < Q ? (p.L - (int64_t)c * Q) : Q);
+  const float A = p.A[head];
+  if (tid == 0) {
+    mbar_init(saddr(&bar_mma), 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) {
+    tmem_alloc(saddr(&tmem_s), Lay::TCOLS);
+    tmem_relinquish();
+  }
+  chunk_prologue<T, Q, K, NT>(p, tok0, head, n, A, s, phi, sred);  // (ends with a barrier)
+
+  // rotated B and C rows e^{-i phi_t} (b.x + i b.y) as f16 hi / lo pairs; zero past the chunk's end
+  for (int i0 = tid; i0 < MR * K; i0 += NT * kLoadBatch) {
+    float2 bv[kLoadBatch], cv[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, m = i / K, k = i % K, t = m / R, r = m % R;
+      bv[u] = cv[u] = make_float2(0.f, 0.f);
+      if (i < MR * K && t < n) {
+        const int64_t o = (((tok0 + t) * p.G + grp) * R + r) * N + 2 * k;
+        bv[u] = ld_pair<T>(p.B, o);
+        cv[u] = ld_pair<T>(p.C, o);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int i = i0 + u * NT, m = i / K, k = i % K, t = m / R;
+      if (i >= MR * K) break;
+      float sn = 0.f, cs = 1.f;
+      if (t < n) sincos_angle(phi[t * K + k], &sn, &cs);
+      const uint32_t o = ((2 * k) / 64) * (MR * 128) + sw128_offset(m, (2 * k) % 64);
+      uint32_t hi, lo;
+      half2_hilo(bv[u].x * cs + bv[u].y * sn, bv[u].y * cs - bv[u].x * sn, hi, lo);
+      *reinterpret_cast<uint32_t*>(sm + Lay::OFF_BHI + o) = hi;
+      *reinterpret_cast<uint32_t*>(sm + Lay::OFF_BLO + o) = lo;
+      half2_hilo(cv[u].x * cs + cv[u].y * sn, cv[u].y * cs - cv[u].x * sn, hi, lo);
+      *reinterpret_cast<uint32_t*>(sm + Lay::OFF_CHI + o) = hi;
+      *reinterpret_cast<uint32_t*>(sm + Lay::OFF_CLO + o) = lo;
+    }
+  }
+  // rows of x (scaled by f_t) or dy (scaled by e^{Lam_t}) as f16 hi / lo pairs
+  auto rows = [&](const auto* src, const float* scale, int off_hi, int off_lo) {
+    using S = typename std::remove_cv<typename std::remove_pointer<decltype(src)>::type>::type;
+    for (int i0 = tid; i0 < MR * P / 2; i0 += NT * kLoadBatch) {
+      float2 v[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int i = i0 + u * NT, m = (2 * i) / P, q = (2 * i) % P, t = m / R;
+        v[u] = (i < MR * P / 2 && t < n) ? ld_pair<S>(src, ((tok0 + t) * p.H + head) * (R * P) + (m % R) * P + q)
+                                         : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int i = i0 + u * NT, m = (2 * i) / P, q = (2 * i) % P, t = m / R;
+        if (i >= MR * P / 2) break;
+        const float sc = t < n ? scale[t] : 0.f;
+        uint32_t hi, lo;
+        half2_hilo(v[u].x * sc, v[u].y * sc, hi, lo);
+        const uint32_t o = sw128_offset(m, q);
+        *reinterpret_cast<uint32_t*>(sm + off_hi + o) = hi;
+        *reinterpret_cast<uint32_t*>(sm + off_lo + o) = lo;
+      }
+    }
+  };
+  rows(static_cast<const T*>(p.x), s.f, Lay::OFF_XHI, Lay::OFF_XLO);
+  for (int k = tid; k < K; k += NT) sPhiEnd[k] = phi[(n - 1) * K + k];
+  __syncthreads();  // the angles are read: dy goes over them
+  rows(p.dy, s.eL, Lay::OFF_YHI, Lay::OFF_YLO);
+  fence_async_smem();  // the tiles, written by these threads, are read by the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+  if (tid == 0) {
+    constexpr uint32_t idesc = idesc_f16_f32(N, P, 1, 1);
+    auto mn = [&](int off, int ks) { return smem_desc(saddr(sm + off) + ks * 2048, MR * 128, 1024, kSwizzle128B); };
+#pragma unroll 1
+    for (int ks = 0; ks < MR / 16; ++ks) {
+      mma_f16(tmem, mn(Lay::OFF_BHI, ks), mn(Lay::OFF_XHI, ks), idesc, ks > 0);
+      mma_f16(tmem, mn(Lay::OFF_BHI, ks), mn(Lay::OFF_XLO, ks), idesc, 1);
+      mma_f16(tmem, mn(Lay::OFF_BLO, ks), mn(Lay::OFF_XHI, ks), idesc, 1);
+      mma_f16(tmem + P, mn(Lay::OFF_CHI, ks), mn(Lay::OFF_YHI, ks), idesc, ks > 0);
+      mma_f16(tmem + P, mn(Lay::OFF_CHI, ks), mn(Lay::OFF_YLO, ks), idesc, 1);
+      mma_f16(tmem + P, mn(Lay::OFF_CLO, ks), mn(Lay::OFF_YHI, ks), idesc, 1);
+    }
+    mma_commit(saddr(&bar_mma));
+  }
+  const bool done = mbar_wait(saddr(&bar_mma), 0, kSumsMaxPolls);
+  tc_fence_after();
+  if (__syncthreads_and(done)) {
+    // warp w: TMEM lane quarter w % 4 (accumulator rows), Z (w < 4) or U
+    const int qtr = warp & 3, which = warp >> 2;
+    const int row = N == 128 ? 32 * qtr + lane : (lane < 16 ? 16 * qtr + lane : -1);
+    const bool re = (lane & 1) == 0;  // rows 2k (re) and 2k + 1 (im) sit in adjacent lanes
+    float sn = 0.f, cs = 1.f;
+    if (which == 0 && row >= 0) sincos_angle(sPhiEnd[row >> 1], &sn, &cs);
+    float2* dst = (which == 0 ? p.Zs : p.Us) + ((int64_t)unit * p.nch + c) * K * P + (row >> 1) * P;
+    // two halves of 32 columns: (re, im) of the first 16 from the re lane
+    // and of the last 16 from the im lane, each a 128-byte run of [K][P][2]
+#pragma unroll 1
+    for (int h0 = 0; h0 < P; h0 += 32) {
+      float v[32];
+#pragma unroll
+      for (int cb = 0; cb < 32; cb += 16) {
+        float w[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * qtr) << 16) + which * P + h0 + cb, w);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[cb + i] = w[i];
+      }
+      tmem_ld_wait();
+      if (which == 0) {  // Z = e^{i phi_end} (Bt^T (f x))
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
+          v[i] = re ? fmaf(v[i], cs, -other * sn) : fmaf(other, sn, v[i] * cs);
+        }
+      }
+      float2 out[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float other = __shfl_xor_sync(0xffffffffu, re ? v[16 + i] : v[i], 1);
+        out[i] = re ? make_float2(v[i], other) : make_float2(other, v[16 + i]);
+      }
+      if (row >= 0) {
+        float2* d = dst + h0 + (re ? 0 : 16);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2)
+          *reinterpret_cast<float4*>(d + i) = make_float4(out[i].x, out[i].y, out[i + 1].x, out[i + 1].y);
+      }
+    }
+  } else {
+    // the products did not complete in time: record it, and give them a
+    // second bounded wait before the tensor memory goes away
+    if (tid == 0) {
+      atomicExch(p.status, 4 /* M3_ERR_TIMEOUT */);
+      mbar_wait(saddr(&bar_mma), 0, kSumsMaxPolls);
+    }
+  }
+  if (tid < K) {
+    const int k = tid;
+    float sn, cs;
+    sincosf(sPhiEnd[k], &sn, &cs);
+    const float e = expf(s.Lam[n - 1]);
+    p.alpha[(int64_t)unit * p.nch * K + (int64_t)c * K + k] = make_float2(e * cs, e * sn);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, Lay::TCOLS);
 }
 
 // ------------------------------------------------------------------ phase 2

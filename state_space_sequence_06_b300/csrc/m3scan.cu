@@ -361,6 +361,23 @@ m3_status m3_test_last_launch(m3_launch_info* out) {
   return M3_OK;
 }
 
+}  // extern "C"
+
+namespace m3 {
+// The device address of the status word, for the backward pass's kernels
+// (built in another translation unit): NULL if it cannot be had.
+int* device_status_word() {
+  void* a = nullptr;
+  if (cudaGetSymbolAddress(&a, g_status) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<int*>(a);
+}
+}  // namespace m3
+
+extern "C" {
+
 m3_status m3_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return M3_ERR_CUDA;
