@@ -133,6 +133,33 @@ __device__ __forceinline__ void block_mm(float (&acc)[TM][TN], int K, FA a, FB b
   }
 }
 
+// The same product when both operands run along k in memory: a(m, k) =
+// A[m SA + k], b(k, j) = B[j SB + k], with SA, SB and K multiples of 4 and
+// 16-byte aligned rows.  Four k per 16-byte load of each operand, the
+// products accumulated in the same order as block_mm.
+template <int TM, int TN, int TY = 16>
+__device__ __forceinline__ void block_mm_k4(float (&acc)[TM][TN], int K, const float* A, int SA, const float* B,
+                                            int SB) {
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 av[TM], bv[TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i) av[i] = *reinterpret_cast<const float4*>(A + (ty + TY * i) * SA + k);
+#pragma unroll
+    for (int j = 0; j < TN; ++j) bv[j] = *reinterpret_cast<const float4*>(B + (tx + 16 * j) * SB + k);
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) {
+        acc[i][j] = fmaf(av[i].x, bv[j].x, acc[i][j]);
+        acc[i][j] = fmaf(av[i].y, bv[j].y, acc[i][j]);
+        acc[i][j] = fmaf(av[i].z, bv[j].z, acc[i][j]);
+        acc[i][j] = fmaf(av[i].w, bv[j].w, acc[i][j]);
+      }
+  }
+}
+
 template <int TM, int TN>
 __device__ __forceinline__ void zero_acc(float (&acc)[TM][TN]) {
 #pragma unroll
@@ -152,7 +179,12 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 template <int N_, int R_>
 struct BwdCfg {
   static constexpr int N = N_, R = R_, P = 64, MR = 64, Q = MR / R, K = N / 2;
-  static constexpr int NS = N + 1, PS = P + 1, MS = MR + 1;  // odd row strides
+  // row strides: NS and PS are multiples of 4 (16-byte row starts for the
+  // four-wide loads of block_mm_k4) that are not multiples of 8 floats, so
+  // the eight lanes of a 16-byte access phase, on eight consecutive rows,
+  // hit eight different 16-byte bank groups; MS is odd (scalar accesses down
+  // a column meet no bank twice)
+  static constexpr int NS = N + 4, PS = P + 4, MS = MR + 1;
   static constexpr int NT = 256;   // chunk sums (two CTAs per SM)
   static constexpr int NTG = 512;  // chunk gradients (one CTA per SM: more warps to hide latency)
   static constexpr int TYG = NTG / 16, TQG = MR / TYG;  // its thread rows, and rows per thread
@@ -756,8 +788,8 @@ __global__ void __launch_bounds__(BwdCfg<N_, R_>::NTG, 1) chunk_grads_kernel(con
   float accS[TQ][TC], accM[TQ][TC];
   zero_acc(accS);
   zero_acc(accM);
-  block_mm<TQ, TC, TY>(accS, N, [&](int m, int k) { return Ct[m * NS + k]; }, [&](int k, int j) { return Bt[j * NS + k]; });
-  block_mm<TQ, TC, TY>(accM, P, [&](int m, int k) { return dY[m * PS + k]; }, [&](int k, int j) { return X[j * PS + k]; });
+  block_mm_k4<TQ, TC, TY>(accS, N, Ct, NS, Bt, NS);
+  block_mm_k4<TQ, TC, TY>(accM, P, dY, PS, X, PS);
 #pragma unroll
   for (int i = 0; i < TQ; ++i)
 #pragma unroll
@@ -914,7 +946,7 @@ __global__ void __launch_bounds__(BwdCfg<N_, R_>::NTG, 1) chunk_grads_kernel(con
     zero_acc(acc);
     zero_acc(acc2);
     block_mm<TQ, TN, TY>(acc, MR, [&](int m, int k) { return T1[m * MS + k]; }, [&](int k, int q) { return Bt[k * NS + q]; });
-    block_mm<TQ, TN, TY>(acc2, P, [&](int m, int k) { return dY[m * PS + k]; }, [&](int k, int q) { return Gs[q * PS + k]; });
+    block_mm_k4<TQ, TN, TY>(acc2, P, dY, PS, Gs, PS);
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
       const float el = s.eL[(ty + TY * i) / R];
@@ -929,7 +961,7 @@ __global__ void __launch_bounds__(BwdCfg<N_, R_>::NTG, 1) chunk_grads_kernel(con
     zero_acc(acc);
     zero_acc(accw);
     block_mm<TQ, TN, TY>(acc, MR, [&](int m, int k) { return T1[k * MS + m]; }, [&](int k, int q) { return Ct[k * NS + q]; });
-    block_mm<TQ, TN, TY>(accw, P, [&](int m, int k) { return X[m * PS + k]; }, [&](int k, int q) { return dG[q * PS + k]; });
+    block_mm_k4<TQ, TN, TY>(accw, P, X, PS, dG, PS);
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
       const int m = ty + TY * i;
