@@ -160,6 +160,32 @@ __device__ __forceinline__ void block_mm_k4(float (&acc)[TM][TN], int K, const f
   }
 }
 
+// Only the first operand along k in memory (a(m, k) = A[m SA + k], SA and
+// K multiples of 4, 16-byte aligned rows): four k per load of A, B read as
+// block_mm does; the same order of accumulation.
+template <int TM, int TN, int TY, class FB>
+__device__ __forceinline__ void block_mm_ak4(float (&acc)[TM][TN], int K, const float* A, int SA, FB b) {
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll 1
+  for (int k = 0; k < K; k += 4) {
+    float4 av[TM];
+#pragma unroll
+    for (int i = 0; i < TM; ++i) av[i] = *reinterpret_cast<const float4*>(A + (ty + TY * i) * SA + k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float bv[TN];
+#pragma unroll
+      for (int j = 0; j < TN; ++j) bv[j] = b(k + u, tx + 16 * j);
+#pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        const float a = u == 0 ? av[i].x : u == 1 ? av[i].y : u == 2 ? av[i].z : av[i].w;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a, bv[j], acc[i][j]);
+      }
+    }
+  }
+}
+
 template <int TM, int TN>
 __device__ __forceinline__ void zero_acc(float (&acc)[TM][TN]) {
 #pragma unroll
@@ -848,7 +874,7 @@ __global__ void __launch_bounds__(BwdCfg<N_, R_>::NTG, 1) chunk_grads_kernel(con
     constexpr int TP = P / 16;
     float acc[TQ][TP];
     zero_acc(acc);
-    block_mm<TQ, TP, TY>(acc, N, [&](int m, int k) { return Ct[m * NS + k]; }, [&](int k, int q) { return Gs[k * PS + q]; });
+    block_mm_ak4<TQ, TP, TY>(acc, N, Ct, NS, [&](int k, int q) { return Gs[k * PS + q]; });
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
       const int m = ty + TY * i;
@@ -885,7 +911,7 @@ __global__ void __launch_bounds__(BwdCfg<N_, R_>::NTG, 1) chunk_grads_kernel(con
     zero_acc(acc);
     zero_acc(acc2);
     block_mm<TQ, TP, TY>(acc, MR, [&](int m, int k) { return T2[k * MS + m]; }, [&](int k, int q) { return dY[k * PS + q]; });
-    block_mm<TQ, TP, TY>(acc2, N, [&](int m, int k) { return Bt[m * NS + k]; }, [&](int k, int q) { return dG[k * PS + q]; });
+    block_mm_ak4<TQ, TP, TY>(acc2, N, Bt, NS, [&](int k, int q) { return dG[k * PS + q]; });
     float dd = 0.f;
 #pragma unroll
     for (int i = 0; i < TQ; ++i) {
