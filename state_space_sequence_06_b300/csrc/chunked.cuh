@@ -316,6 +316,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   __shared__ float sPhi[2][K2];
   __shared__ float sBScl[MR], sCScl[MR];  // BC norm: 1 / rms of each (token, rank) row of the tile
   __shared__ float sCarryScl[8];          // BC norm of the carried B rows at a segment start
+  __shared__ __nv_bfloat16 sCarryX[R * 64];  // the carried x rows at a segment start
   __shared__ float sPhiEndX[XB][K2];  // the same after chunk c (slot c % XB), for the state warps
 
   // this CTA's segments: {unit, first token, end token, flags}, the first
@@ -879,7 +880,20 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           const float sc = warp_rms_scale(cB + r * N, N, tt & 31);
           if ((tt & 31) == 0) sCarryScl[r] = sc;
         }
-        group_sync(2, NSTA);
+      }
+      // the carry's B entries of this thread's row (scaled by beta'_0) and
+      // the carried x rows (into shared memory): read once, not per column
+      // block, so that the column loop waits only on the state's loads
+      float cbr[R];
+      if (cB) {
+        for (int i = tt; i < R * P; i += NSTA) sCarryX[i] = cx[i];
+#pragma unroll
+        for (int r = 0; r < R; ++r) cbr[r] = g_row >= 0 ? __bfloat162float(cB[r * N + g_row]) : 0.f;
+      }
+      if (norm_c || cB) group_sync(2, NSTA);
+      if (cB) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) cbr[r] *= bet0 * (norm_c ? sCarryScl[r] : 1.f);
       }
       for (int cb = 0; cb < P; cb += 16) {
         float v[16];
@@ -913,14 +927,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             v[8 + i] = re ? other : mine;
           }
         }
-        if (g_row >= 0) {
-          if (cB) {
-            for (int r = 0; r < R; ++r) {
-              const float b = bet0 * (norm_c ? sCarryScl[r] : 1.f) * __bfloat162float(cB[r * N + g_row]);
-              const __nv_bfloat16* xp = cx + r * P + cb;
+        if (g_row >= 0 && cB) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = fmaf(b, __bfloat162float(xp[i]), v[i]);
-            }
+          for (int r = 0; r < R; ++r) {
+            const __nv_bfloat16* xp = sCarryX + r * P + cb;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = fmaf(cbr[r], __bfloat162float(xp[i]), v[i]);
           }
         }
         tmem_st16(tmem + lane_base + Cfg::COL_G + cb, v);
