@@ -834,6 +834,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const bool from_slot = (sg.w & SEG_SRC_SLOT) != 0;
       const bool split = (sg.w & SEG_SPLIT) != 0;
       const int slot = sg.w >> 8;
+      // the first token's dt and lam, loaded before the wait below (their
+      // latency overlaps it)
+      const int64_t row0 = sSegTok0[si] * H + head;
+      const __nv_bfloat16 dt0_raw = p.dt[row0];
+      const __nv_bfloat16 lm0_raw = p.lam ? p.lam[row0] : __float2bfloat16(1.f);  // no lam: lam = 1
       if (from_slot && !split) {  // bounded wait for the CTA that runs the first part of this unit
         bool ok = false;
         const uint64_t t0 = globaltimer_ns();
@@ -870,9 +875,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           cx = p.prev_x ? (SO ? p.prev_x + (int64_t)unit * R * P : p.xx + (int64_t)slot * R * P) : nullptr;
         }
       }
-      const int64_t row0 = sSegTok0[si] * H + head;
-      const float dt0 = scan_dt(__bfloat162float(p.dt[row0]), p.pro, p.dt_bias, head);
-      const float lm0 = p.lam ? __bfloat162float(p.lam[row0]) : 1.f;
+      const float dt0 = scan_dt(__bfloat162float(dt0_raw), p.pro, p.dt_bias, head);
+      const float lm0 = __bfloat162float(lm0_raw);
       const float bet0 = (1.f - lm0) * dt0;
       const bool norm_c = (p.pro & M3_PRO_BC_NORM) && cB;  // BC norm of the carried B rows
       if (norm_c) {
@@ -895,29 +899,37 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
 #pragma unroll
         for (int r = 0; r < R; ++r) cbr[r] *= bet0 * (norm_c ? sCarryScl[r] : 1.f);
       }
-      for (int cb = 0; cb < P; cb += 16) {
-        float v[16];
+      // the 16 columns of pair g_row / 2 are 128 contiguous bytes (re, im
+      // interleaved): the re lane loads columns cb..cb+7, the im lane
+      // cb+8..cb+15, and each passes the other the half it needs; the next
+      // block's loads are issued before this block's are used
+      const bool re = (g_row & 1) == 0;
+      auto load_own = [&](int cb, float (&o)[16]) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-        if (h0) {
-          // the 16 columns of pair g_row / 2 are 128 contiguous bytes (re, im
-          // interleaved): the re lane loads columns cb..cb+7, the im lane
-          // cb+8..cb+15, and each passes the other the half it needs
-          const bool re = (g_row & 1) == 0;
-          float own[16];
+        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        if (h0 && g_row >= 0) {
+          const float4* hs = reinterpret_cast<const float4*>(h0 + (int64_t)(g_row >> 1) * P * 2 + (cb + (re ? 0 : 8)) * 2);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) own[i] = 0.f;
-          if (g_row >= 0) {
-            const float4* hs = reinterpret_cast<const float4*>(h0 + (int64_t)(g_row >> 1) * P * 2 + (cb + (re ? 0 : 8)) * 2);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float4 f = hs[q];
-              own[4 * q] = f.x;
-              own[4 * q + 1] = f.y;
-              own[4 * q + 2] = f.z;
-              own[4 * q + 3] = f.w;
-            }
+          for (int q = 0; q < 4; ++q) {
+            const float4 f = hs[q];
+            o[4 * q] = f.x;
+            o[4 * q + 1] = f.y;
+            o[4 * q + 2] = f.z;
+            o[4 * q + 3] = f.w;
           }
+        }
+      };
+      float nxt[16];
+      load_own(0, nxt);
+      for (int cb = 0; cb < P; cb += 16) {
+        float v[16], own[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          v[i] = 0.f;
+          own[i] = nxt[i];
+        }
+        if (cb + 16 < P) load_own(cb + 16, nxt);
+        if (h0) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             // (selects, not lane-dependent indices, keep the arrays in registers)
