@@ -403,11 +403,14 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   const int nchunks = sSegC0[nseg];
   if (nchunks == 0) return;  // nothing to do; the state slot keeps its contents
   // segment of chunk c of this CTA's stream (a handful of entries)
-  auto seg_of = [&](int c) {
-    int si = 0;
+  // (from segment si0 on: the roles walk their chunks in order, so the
+  // segment they were last in is where the search starts)
+  auto seg_from = [&](int c, int si0) {
+    int si = si0;
     while (si + 1 < nseg && c >= sSegC0[si + 1]) ++si;
     return si;
   };
+  auto seg_of = [&](int c) { return seg_from(c, 0); };
   auto seg_head = [&](int si) { return sSegHead[si]; };
   auto seg_ntok = [&](int si) { return (int64_t)(sSeg[si].z - sSeg[si].y); };
   auto seg_last = [&](int c) { return c + 1 == sSegC0[seg_of(c) + 1]; };
@@ -483,11 +486,12 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // must stay 0, not become softplus(bias))
     constexpr uint32_t kNoToken = 0xFFFFFFFFu;
     const bool dt_sp = (p.pro & M3_PRO_DT_SOFTPLUS) != 0;
+    int pro_si = 0;  // the segment of the prologue's last chunk
     auto load_scalars = [&](int c, uint32_t& d, uint32_t& l, int tok) {
       d = dt_sp ? kNoToken : 0u;
       l = 0u;
       if (tok <= Q && c < nchunks) {
-        const int si = seg_of(c);
+        const int si = seg_from(c, pro_si);
         const int64_t i = (int64_t)(c - sSegC0[si]) * Q + tok;
         if (i < seg_ntok(si)) {
           const int64_t row = (sSegTok0[si] + i) * H + seg_head(si);
@@ -504,7 +508,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       constexpr bool NORM = decltype(normtag)::value;
       const int s = c % NS, xs = c % XB;  // stage, scalar slot
       uint8_t* stg = stage(s);
-      const int si = seg_of(c);
+      const int si = seg_from(c, pro_si);
+      pro_si = si;
       const float A = sSegA[si];
       // a segment starts from the phase 0 (its initial state is un-rotated);
       // these threads also wrote the previous chunk's phase
