@@ -181,13 +181,21 @@ class ClockSampler:
             return self
         self.stop = threading.Event()
         ct, lib, h = self.ct, self.lib, self.h
+        sm, rs = ct.c_uint(), ct.c_ulonglong()
+
+        def sample():
+            if lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ct.byref(sm)) == 0 and \
+                    self.get_reasons(h, ct.byref(rs)) == 0:
+                self.samples.append((sm.value, rs.value))
+
+        # the first queries of a process are slow: take them here, before the
+        # caller's timed region starts, and keep only the thread's samples
+        sample()
+        self.samples.clear()
 
         def run():
-            sm, rs = ct.c_uint(), ct.c_ulonglong()
             while not self.stop.is_set():
-                if lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ct.byref(sm)) == 0 and \
-                        self.get_reasons(h, ct.byref(rs)) == 0:
-                    self.samples.append((sm.value, rs.value))
+                sample()
                 self.stop.wait(self.period)
 
         self.th = threading.Thread(target=run, daemon=True)
