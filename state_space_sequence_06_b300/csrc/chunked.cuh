@@ -39,7 +39,12 @@
 // hi*hi, hi*lo and lo*hi terms, so those operands keep about 21 bits: one
 // f16 rounding (11 bits) is not enough for outputs 20-40x the rms of y,
 // which the tails of the dt distribution produce.  Only the state copy R
-// that feeds the inter-chunk output stays a single f16.
+// that feeds the inter-chunk output stays a single f16.  S' is written
+// over its own scores in TMEM (each 16-column block of f32 S becomes 8
+// columns of packed f16 hi words and 8 of lo words) and read from there by
+// MMA 2 as its A operand; inside each block of 16 K rows, MMA 2 sees the
+// columns of S' in the order kperm gives, and the f16 copy of X takes its
+// rows in the same order.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap and its enums (types only: the driver entry point is looked up at run time)
@@ -169,18 +174,18 @@ struct ChunkCfg {
   static constexpr uint32_t STAGE_TX = 2 * CT_BYTES + XT_BYTES + (RE ? 0 : TH_BYTES);
   // outside the stages: X in f16 (it lives until the output of its chunk,
   // so it and the per-chunk scalars rotate through XB slots: three when they
-  // fit), S' hi and lo (K-major), R (MN-major)
-  static constexpr int ST_BYTES = MR * MR * 2, RT_BYTES = N * P * 2;
-  static constexpr int smem_for(int xb) { return 2 * STAGE + xb * XT_BYTES + 2 * ST_BYTES + RT_BYTES + 1024; }
+  // fit) and R (MN-major); S' lives in TMEM
+  static constexpr int RT_BYTES = N * P * 2;
+  static constexpr int smem_for(int xb) { return 2 * STAGE + xb * XT_BYTES + RT_BYTES + 1024; }
   static constexpr int STATIC_EST = 3 * 6 * Q * 4 + (NPRO / K2) * K2 * 4 + 2048;  // scalars, scan, misc
   static constexpr int XB = smem_for(3) + STATIC_EST <= 232448 ? 3 : 2;
-  static constexpr int OFF_XB = 2 * STAGE, OFF_ST = OFF_XB + XB * XT_BYTES, OFF_STLO = OFF_ST + ST_BYTES;
-  static constexpr int OFF_RT = OFF_STLO + ST_BYTES;
+  static constexpr int OFF_XB = 2 * STAGE;
+  static constexpr int OFF_RT = OFF_XB + XB * XT_BYTES;
   static constexpr int SMEM = OFF_RT + RT_BYTES + 1024;  // + alignment slack
   // state-only pass: a stage without its C tiles (from the B tiles on)
   static constexpr int SO_STRIDE = STAGE - OFF_B;
   static_assert(SMEM + STATIC_EST <= 232448, "shared memory of one CTA");
-  // TMEM columns (f32): S[2], Y[2], Yi[2], state, chunk-local state
+  // TMEM columns (f32): S[2] (then S' in place), Y[2], Yi[2], state, chunk-local state
   static constexpr int COL_S = 0, COL_Y = 2 * MR, COL_YI = 2 * MR + 2 * P, COL_G = 2 * MR + 4 * P;
   static constexpr int COL_SC = COL_G + P;  // the chunk-local state B^T (W X) of MMA 4
   // its second buffer in the state-only pass, which has no S, Y or Yi
@@ -211,6 +216,14 @@ __device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint
 
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// Row of the f16 copy of X that holds row j of X.  Inside each block of 16
+// rows it is the K position at which MMA 2 reads column j of S' from TMEM:
+// S -> S' stores the columns 8 g + 2 m + e (g, e < 2, m < 4) of a block as
+// the f16 pair of word column 2 m + g, which holds K positions 4 m + 2 g + e.
+__host__ __device__ constexpr int kperm(int j) {
+  return (j & ~15) | (((j & 7) >> 1) << 2) | (((j >> 3) & 1) << 1) | (j & 1);
 }
 
 // sin and cos of x after one reduction step by 2*pi (|x| stays within a few
@@ -285,7 +298,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   // read where a segment ends), opready (prologue done), free (stage no longer
   // read by MMAs), xready (X of the slot's chunk converted), xfree (X slot and
   // output accumulators no longer read), sfull (MMA 1 done), yfull (MMAs 2
-  // and 3 done), spready (S' written), scfull (MMA 4 done: the chunk-local
+  // and 3 done), spready (S' of the buffer written), scfull (MMA 4 done: the chunk-local
   // state is in TMEM), scfree (the state warps have folded it into the
   // state), stready (R, the f16 copy of the state for MMA 3, written; once
   // before the first chunk and once per chunk), rfree (MMA 3 done reading
@@ -293,9 +306,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   // phases behind the barrier; each pairing below is chained so that it
   // cannot.
   // (full, opready and free per stage: NS of them)
-  __shared__ __align__(8) uint64_t bar_full[3], bar_opready[3], bar_free[3], bar_sfull[2], bar_yfull[2];
+  __shared__ __align__(8) uint64_t bar_full[3], bar_opready[3], bar_free[3], bar_sfull[2], bar_yfull[2], bar_spready[2];
   __shared__ __align__(8) uint64_t bar_xfree[XB], bar_xready[XB], bar_phend[XB];
-  __shared__ __align__(8) uint64_t bar_spready, bar_stready, bar_rfree;
+  __shared__ __align__(8) uint64_t bar_stready, bar_rfree;
   // scfull / scfree per chunk-local state buffer: one buffer (index 0) in the
   // full pass; two in the state-only pass, chunk c in buffer c & 1, so MMA 4
   // of chunk c + 1 does not wait for the state step of chunk c
@@ -416,8 +429,6 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   auto seg_last = [&](int c) { return c + 1 == sSegC0[seg_of(c) + 1]; };
   volatile CtaAbort* abort_flag = &s_abort;
 
-  uint8_t* St = sm + Cfg::OFF_ST;
-  uint8_t* Stlo = sm + Cfg::OFF_STLO;
   uint8_t* Rt = sm + Cfg::OFF_RT;
   // Stages: two in the full pass; three in the state-only pass, whose stages
   // hold no C tiles (stage s there starts OFF_B bytes before its B tiles,
@@ -442,6 +453,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
+      mbar_init(saddr(&bar_spready[s]), 1);
     }
     for (int x = 0; x < XB; ++x) {
       // MMA 2 completion and the output epilogue (SO: the state warps, once
@@ -450,7 +462,6 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X (not in SO)
       mbar_init(saddr(&bar_phend[x]), K2);  // the phase after the slot's chunk, one arrival per pair
     }
-    mbar_init(saddr(&bar_spready), 1);
     mbar_init(saddr(&bar_stready), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(saddr(&bar_scfull[b]), 1);
@@ -726,13 +737,13 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       l_cur = l_nxt;
       return true;
     };
-    // S -> S' of chunk c (after MMA 1 of c, and after MMA 2 of c - 1 has read S')
+    // S -> S' of chunk c (after MMA 1 of c), in place in S[c & 1]: MMA 2 of
+    // chunk c - 2, the last reader of that buffer's S', was issued before
+    // MMA 1 of chunk c by the same thread
     auto scores = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       const float lam_end = sLamEnd[xs];
-      bool got = wait_or_abort(saddr(&bar_sfull[s]), (uint32_t)((c >> 1) & 1), abort_flag);
-      if (got && c >= 1)
-        got = wait_or_abort(saddr(&bar_yfull[(c - 1) & 1]), (uint32_t)(((c - 1) >> 1) & 1), abort_flag);
+      const bool got = wait_or_abort(saddr(&bar_sfull[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       // (the vote on `got` is taken at the closing barrier, as in the prologue)
       tc_fence_after();
       // warp w covers accumulator rows 16(w%4) .. +15 (TMEM lane quarter w%4)
@@ -752,63 +763,60 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       const int cl = 2 * (lane % 4);        // this thread's column pair inside each 8-column group
 #pragma unroll 1
       for (int cb = 0; cb < CPH; cb += 16) {
-        if ((cbeg + cb) / R > it_warp) break;  // this and later column blocks: all masked, zeros in place
-        float sv[8];  // [group gg][4]: (r0, c), (r0, c+1), (r0+8, c), (r0+8, c+1)
-        tmem_ld16x256b_x2(tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb, sv);
-        tmem_ld_wait();
+        const uint32_t ta = tmem + lane_base + Cfg::COL_S + s * MR + cbeg + cb;
+        // the block's S' as 8 columns of hi words, then 8 of lo words; the
+        // word of columns (8 gg + cl, +1) of each row goes to word column
+        // cl + gg (the 16x256b store puts this thread's registers 2i, 2i + 1
+        // of each group at word columns cl, cl + 1), which is the order kperm
+        // describes
+        uint32_t wv[8];  // [hi, lo][(r0, gg 0), (r0, gg 1), (r0 + 8, gg 0), (r0 + 8, gg 1)]
+        if ((cbeg + cb) / R > it_warp) {  // all masked: zeros
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          const int j = cbeg + cb + 8 * gg + cl;  // first of this thread's two columns
-          float bw2[2];
-          if (R == 1) {
-            const float2 w2 = *reinterpret_cast<const float2*>(&sBw[xs][j]);
-            bw2[0] = w2.x;
-            bw2[1] = w2.y;
-          } else {
-            bw2[0] = sBw[xs][j / R];
-            bw2[1] = sBw[xs][(j + 1) / R];
-          }
-          uint32_t hv[2], lv[2];
+          for (int i = 0; i < 8; ++i) wv[i] = 0u;
+        } else {
+          float sv[8];  // [group gg][4]: (r0, c), (r0, c+1), (r0+8, c), (r0+8, c+1)
+          tmem_ld16x256b_x2(ta, sv);
+          tmem_ld_wait();
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int it = rr ? it1 : it0;
-            const float elam_t = rr ? elam1 : elam0, lam_t = rr ? lam1 : lam0, gam_t = rr ? gam1 : gam0;
-            float e[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int jt = (j + u) / R;
-              const float sij = sv[4 * gg + 2 * rr + u];
-              const float off = factor ? sij * bw2[u] * elam_t : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
-              e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
+          for (int gg = 0; gg < 2; ++gg) {
+            const int j = cbeg + cb + 8 * gg + cl;  // first of this thread's two columns
+            float bw2[2];
+            if (R == 1) {
+              const float2 w2 = *reinterpret_cast<const float2*>(&sBw[xs][j]);
+              bw2[0] = w2.x;
+              bw2[1] = w2.y;
+            } else {
+              bw2[0] = sBw[xs][j / R];
+              bw2[1] = sBw[xs][(j + 1) / R];
             }
-            split_half2(e[0], e[1], hv[rr], lv[rr]);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const int it = rr ? it1 : it0;
+              const float elam_t = rr ? elam1 : elam0, lam_t = rr ? lam1 : lam0, gam_t = rr ? gam1 : gam0;
+              float e[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int jt = (j + u) / R;
+                const float sij = sv[4 * gg + 2 * rr + u];
+                const float off = factor ? sij * bw2[u] * elam_t : sij * __expf(lam_t - sLam[xs][jt]) * sWp[xs][jt];
+                e[u] = jt < it ? off : (jt == it ? sij * gam_t : 0.f);
+              }
+              split_half2(e[0], e[1], wv[2 * rr + gg], wv[4 + 2 * rr + gg]);
+            }
           }
-          const uint32_t o0 = (j / 64) * (MR * 128) + sw128_offset(r0, j % 64);
-          const uint32_t o1 = (j / 64) * (MR * 128) + sw128_offset(r0 + 8, j % 64);
-          *reinterpret_cast<uint32_t*>(St + o0) = hv[0];
-          *reinterpret_cast<uint32_t*>(Stlo + o0) = lv[0];
-          *reinterpret_cast<uint32_t*>(St + o1) = hv[1];
-          *reinterpret_cast<uint32_t*>(Stlo + o1) = lv[1];
         }
+        tmem_st16x256b_x2(ta, wv);
       }
+      tmem_st_wait();
       tc_fence_before();
-      fence_async_smem();
       if (!group_and(1, NPRO, got)) return false;
-      if (pt == 0) mbar_arrive(saddr(&bar_spready));
+      if (pt == 0) mbar_arrive(saddr(&bar_spready[s]));
       return true;
     };
     // the prologue runs one chunk ahead of S -> S', which waits for MMA 1
     // compiled once with and once without the BC norm (the real-state
     // variant has none: its B and C reach the MMAs without a lo part)
     auto run = [&](auto normtag) {
-      // S' blocks above the diagonal are zero in every chunk: written once
-      // here and skipped by S -> S' (ordered before MMA 2 by the first
-      // S -> S' barrier)
-      if (!SO) {
-        for (int i = pt; i < 2 * Cfg::ST_BYTES / 16; i += NPRO)
-          reinterpret_cast<uint4*>(St)[i] = make_uint4(0u, 0u, 0u, 0u);  // (Stlo follows St)
-        fence_async_smem();
-      }
       bool alive = prologue(0, normtag);
       for (int c = 0; c < nchunks && alive; ++c) {
         if (c + 1 < nchunks && !prologue(c + 1, normtag)) break;
@@ -1074,7 +1082,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
             hx[q] = pack_half2(f.x, f.y);
             split_half2(w * f.x, w * f.y, hw[q], lw[q]);
           }
-          if (!SO) *reinterpret_cast<uint4*>(Xb + o) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
+          if (!SO)
+            *reinterpret_cast<uint4*>(Xb + sw128_offset(kperm(row), c8 * 8)) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
           *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
@@ -1177,7 +1186,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           const int col = 32 * half + 8 * g8 + cl;
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
-            const uint32_t xv = *reinterpret_cast<const uint32_t*>(Xb + sw128_offset(r0 + 8 * rr, col));
+            const uint32_t xv = *reinterpret_cast<const uint32_t*>(Xb + sw128_offset(kperm(r0 + 8 * rr), col));
             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xv));
             const int i0 = 4 * g8 + 2 * rr;
             const float o0 = fmaf(Dh, f.x, fmaf(el[rr], b[i0], a[i0]));
@@ -1239,7 +1248,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
         const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
         if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) return false;
-        // S[s] was last read by S -> S' of chunk c - 2, which MMA 2 of chunk c - 2 already waited for
+        // S[s] last held the S' of chunk c - 2: MMA 2 of that chunk, issued
+        // before this by this thread, read it (tcgen05 MMAs of one thread run
+        // in issue order), after S -> S' of chunk c - 2 was done
         tc_fence_after();
         // S = C B^T = Chi Bhi^T + Chi Blo^T + Clo Bhi^T   (M = MR, N = MR, K = N)
         constexpr uint32_t idesc = idesc_f16_f32(MR, MR, 0, 0);
@@ -1261,17 +1272,19 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       for (int c = 0; c < nchunks && alive; ++c) {
         const int s = c & 1;
         if (c + 1 < nchunks && !mma1(c + 1)) break;
-        if (!wait_or_abort(saddr(&bar_spready), (uint32_t)(c & 1), abort_flag)) break;
+        if (!wait_or_abort(saddr(&bar_spready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) break;
         if (!wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;  // X of chunk c
         if (c >= 2 && !wait_xfree(c - 2)) break;  // Y[s] last held the output of chunk c - 2
         tc_fence_after();
-        // Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16)
+        // Y[s] = S' X = S'hi X + S'lo X   (M = MR, N = P, K = MR; X is exact in f16):
+        // S' from TMEM (K step ks: 8 columns of hi words at 16 ks, then 8 of lo)
         const uint32_t Xb = saddr(xbuf(c % XB));
+        const uint32_t sp = tmem + Cfg::COL_S + s * MR;
         constexpr uint32_t idesc = idesc_f16_f32(MR, P, 0, 1);
 #pragma unroll 1
         for (int ks = 0; ks < MR / 16; ++ks) {
-          mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(St), ks, MR * 128), mnmaj(Xb, ks, MR * 128), idesc, ks > 0);
-          mma_f16(tmem + Cfg::COL_Y + s * P, kmaj(saddr(Stlo), ks, MR * 128), mnmaj(Xb, ks, MR * 128), idesc, 1);
+          mma_f16_ta(tmem + Cfg::COL_Y + s * P, sp + 16 * ks, mnmaj(Xb, ks, MR * 128), idesc, ks > 0);
+          mma_f16_ta(tmem + Cfg::COL_Y + s * P, sp + 16 * ks + 8, mnmaj(Xb, ks, MR * 128), idesc, 1);
         }
         mma_commit(saddr(&bar_yfull[s]));
         mma_commit(saddr(&bar_xfree[c % XB]));

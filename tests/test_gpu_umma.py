@@ -1,6 +1,7 @@
 """The tcgen05 operand and accumulator layouts the chunked kernel relies
 on, checked on the GPU against torch: 128B-swizzled K-major and MN-major
-f16 operands, M = 64 and M = 128 accumulators in TMEM."""
+f16 operands, M = 64 and M = 128 accumulators in TMEM, and an A operand
+read from TMEM (the kernel's S')."""
 import ctypes
 import os
 import subprocess
@@ -23,6 +24,13 @@ class ProbeArgs(ctypes.Structure):
                 ("out2", ctypes.c_void_p)]
 
 
+class ProbeTaArgs(ctypes.Structure):
+    _fields_ = [("a_words", ctypes.c_void_p), ("b_img", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("err", ctypes.c_void_p), ("b_lbo", ctypes.c_uint32), ("b_sbo", ctypes.c_uint32),
+                ("b_kstep", ctypes.c_uint32), ("nk", ctypes.c_int), ("idesc", ctypes.c_uint32),
+                ("ncols", ctypes.c_int), ("a_col", ctypes.c_int), ("a_kstep", ctypes.c_int)]
+
+
 @pytest.fixture(scope="module")
 def probe(tmp_path_factory):
     so = str(tmp_path_factory.mktemp("umma") / "probe.so")
@@ -31,6 +39,7 @@ def probe(tmp_path_factory):
                            os.path.join(HERE, "umma_probe.cu")])
     lib = ctypes.CDLL(so)
     lib.umma_probe_run.argtypes = [ctypes.POINTER(ProbeArgs)]
+    lib.umma_probe_ta_run.argtypes = [ctypes.POINTER(ProbeTaArgs)]
     return lib
 
 
@@ -160,3 +169,31 @@ def test_ld_16x256b_layout(probe):
                     lane = 32 * w + t // 4 + 8 * (q // 2)
                     col = 16 * cb + 8 * j + 2 * (t % 4) + (q % 2)
                     assert o2[w, cb, t, i] == got[lane, col], (w, cb, t, i)
+
+
+@pytest.mark.parametrize("M", [64, 128])
+def test_a_from_tmem(probe, M):
+    """A read from TMEM (kind::f16, K-major): row r in the accumulator's lane
+    for row r at that M, two f16 of K per 32-bit column (the lower K in the
+    low half), a K = 16 step every 8 columns.  Lanes that hold no row carry
+    1000s, so a read of them would show."""
+    N, K = 64, 64
+    A, B = rand((M, K), 13), rand((N, K), 14)
+    lane = (lambda r: r) if M == 128 else (lambda r: (r // 16) * 32 + r % 16)
+    words = np.full((128, 32), 0x63D063D0, np.uint32)
+    a16 = A.astype(np.float16).view(np.uint16).astype(np.uint32)
+    for r in range(M):
+        words[lane(r)] = a16[r, 0::2] | (a16[r, 1::2] << 16)
+    bo, _, bstep = kmajor_image(N, K)
+    b_img = np.zeros(65536, np.uint8)
+    b_img.view(np.float16)[(bo // 2).ravel()] = B.astype(np.float16).ravel()
+    tw, tb = torch.from_numpy(words.view(np.int32)).cuda(), torch.from_numpy(b_img).cuda()
+    out = torch.full((128, N), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = ProbeTaArgs(tw.data_ptr(), tb.data_ptr(), out.data_ptr(), err.data_ptr(), 16, 1024, bstep(1), K // 16,
+                       idesc(M, N, 0, 0), N, 128, 8)
+    assert probe.umma_probe_ta_run(ctypes.byref(args)) == 0
+    assert err.item() == 0, "mbarrier wait timed out"
+    got = out.cpu().numpy()
+    rows = [lane(r) for r in range(M)]
+    np.testing.assert_allclose(got[rows], A @ B.T, rtol=0, atol=1e-5)
