@@ -189,18 +189,32 @@ class ClockSampler:
                 self.samples.append((sm.value, rs.value))
 
         # the first queries of a process are slow: take them here, before the
-        # caller's timed region starts, and keep only the thread's samples
+        # caller's timed region starts, and keep only the later samples
         sample()
         self.samples.clear()
+        self._sample = sample
+
+        started = threading.Event()
 
         def run():
             while not self.stop.is_set():
                 sample()
+                started.set()
                 self.stop.wait(self.period)
 
+        # the caller's timed region starts once the thread runs its loop (its
+        # start-up then takes no host time from the first launch)
         self.th = threading.Thread(target=run, daemon=True)
         self.th.start()
+        started.wait(0.5)
         return self
+
+    def restart(self):
+        """Drop the samples taken so far (those before a timed region) and
+        take one at its start."""
+        if self.err is None:
+            self.samples.clear()
+            self._sample()
 
     def __exit__(self, *a):
         if self.err is None:
@@ -484,12 +498,16 @@ def measure(wl, args, m3, torch, dist, world, local, stream, headline):
         except Exception as e:  # reported, never hides a number
             parity = {"error": repr(e)[:200]}
 
-    warm_up(step, args.warmup, torch)
-    ev_pairs.clear()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    # the sampler starts before the warm-up, so that the device does not idle
+    # between the warm-up and the timed region; its samples are those of the
+    # timed region
     with ClockSampler(local) as clk:
+        warm_up(step, args.warmup, torch)
+        ev_pairs.clear()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.restart()
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
         g0.record(stream)
@@ -701,10 +719,11 @@ def run_backward(wl, args, m3, torch, dist, world, rank, local, stream):
     def warm():
         box["out"] = once()
 
-    warm_up(warm, args.warmup, torch)
-    out = box["out"]
     steps = args.steps if algo != m3.M3_ALGO_RECURRENT else min(args.steps, 3)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk:  # (started before the warm-up, as in measure())
+        warm_up(warm, args.warmup, torch)
+        out = box["out"]
+        clk.restart()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
