@@ -151,6 +151,7 @@ struct ChunkCfg {
   // and 3).  The prologue's work is latency-bound: more warps hide more of it.
   static constexpr int NPRO = R == 1 ? 512 : 256, NSTA = 128, NT = NPRO + NSTA + 96;
   static constexpr int W_STA = NPRO / 32, W_MMA = W_STA + NSTA / 32, W_TMA = W_MMA + 1, W_MMA2 = W_TMA + 1;
+
   // rotation work split: consecutive threads take consecutive pairs (so
   // shared-memory rows are read without bank conflicts), G token groups
   static constexpr int G = NPRO / K2, TPG = Q / G;
@@ -283,7 +284,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // SO: the state-only pass of the split schedule: no C, no scores, no
 // outputs; MMA 4 and the state chain only, each segment's final state and
 // total decay and rotation to seg_h / seg_alpha.
-template <int N, int R, int Q, bool RE, bool SO = false>
+// XC: the prologue warps convert X to f16 and form W X (the full pass at
+// rank 1), instead of the state warps.
+template <int N, int R, int Q, bool RE, bool SO = false, bool XC = false>
 __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
                            const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_th,
@@ -428,6 +431,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   auto seg_ntok = [&](int si) { return (int64_t)(sSeg[si].z - sSeg[si].y); };
   auto seg_last = [&](int c) { return c + 1 == sSegC0[seg_of(c) + 1]; };
   volatile CtaAbort* abort_flag = &s_abort;
+  constexpr bool xc_pro = XC && !SO && R == 1;
 
   uint8_t* Rt = sm + Cfg::OFF_RT;
   // Stages: two in the full pass; three in the state-only pass, whose stages
@@ -603,14 +607,16 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       }
       group_sync(1, NPRO);  // sLam and sPsum complete
       const float lam_end = sLam[xs][Q - 1];
-      if constexpr (SO) {
+      if constexpr (SO || xc_pro) {
         // ---- the state-only pass has no C to rotate and no scores: these
         //      warps also form W X as hi (over x) and lo (over theta, read
         //      above) parts for MMA 4, W_j = e^{Lam_end - Lam_j} (gamma_j +
         //      beta'_{j+1}), so that the stage's operands are ready with
-        //      the prologue
+        //      the prologue (and in the full pass, where they take this
+        //      work, the f16 copy of X)
         uint8_t* Xs = stg + Cfg::OFF_X;
         uint8_t* WXlo = stg + Cfg::OFF_WXLO;
+        uint8_t* Xb = xbuf(xs);
 #pragma unroll 1
         for (int idx = pt; idx < MR * (P / 8); idx += NPRO) {
           const int row = idx / (P / 8), c8 = idx % (P / 8), j = row / R;
@@ -618,12 +624,15 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           const uint4 raw = *reinterpret_cast<const uint4*>(Xs + o);
           const float w = __expf(lam_end - sLam[xs][j]) * (sGam[xs][j] + sBet[j + 1]);
           const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t hw[4], lw[4];
+          uint32_t hx[4], hw[4], lw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float2 f = bf2_to_f2(rw[q]);
+            hx[q] = pack_half2(f.x, f.y);
             split_half2(w * f.x, w * f.y, hw[q], lw[q]);
           }
+          if (!SO)
+            *reinterpret_cast<uint4*>(Xb + sw128_offset(kperm(row), c8 * 8)) = make_uint4(hx[0], hx[1], hx[2], hx[3]);
           *reinterpret_cast<uint4*>(Xs + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(WXlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
@@ -732,7 +741,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (g == 0) sPhi[pb ^ 1][k] = sPhiEndX[xs][k];
       fence_async_smem();
       if (!group_and(1, NPRO, got)) return false;
-      if (pt == 0) mbar_arrive(saddr(&bar_opready[s]));
+      if (pt == 0) {
+        mbar_arrive(saddr(&bar_opready[s]));
+        if constexpr (xc_pro) mbar_arrive(saddr(&bar_xready[xs]));
+      }
       d_cur = d_nxt;
       l_cur = l_nxt;
       return true;
@@ -1217,7 +1229,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         if (!init_seg(si)) break;
         const int end = sSegC0[si + 1];
         for (; n < end; ++n) {
-          if ((!SO && !xconv(n)) || (!SO && n >= 1 && !output(n - 1, ybf)) || !state(n)) {
+          if ((!SO && !xc_pro && !xconv(n)) || (!SO && n >= 1 && !output(n - 1, ybf)) || !state(n)) {
             alive = false;
             break;
           }
@@ -1611,8 +1623,14 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
   p.dt_bias = a->dt_bias;
   p.wait_ns = test_hooks().wait_ns.load();
   p.fault = test_hooks().fault.load();
-  auto kern = chunked_prefill_kernel<N, R, Q, RE>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
+  // X converted by the prologue warps at rank 1 without the BC norm (there
+  // they have room for it; with the norm, at rank > 1 and in the split
+  // schedule the state warps do it: measured faster each way)
+  auto kern_sx = chunked_prefill_kernel<N, R, Q, RE>;
+  auto kern = (R == 1 && !(a->prologue & M3_PRO_BC_NORM)) ? chunked_prefill_kernel<N, R, Q, RE, false, R == 1>
+                                                          : kern_sx;
+  if (cudaFuncSetAttribute(kern_sx, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return M3_ERR_CUDA;
   const int units = nseq * H;
   // Split schedule: with fewer units than SMs (one long sequence of a few
@@ -1660,7 +1678,7 @@ m3_status chunked_launch(const m3_prefill_args* a, float* h, void* prev_B, void*
           p.seg_alpha = reinterpret_cast<float2*>(b8 + o_sa);
           kso<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
           split_combine_kernel<N, R, Q><<<dim3((N / 2) * 64 / 256, (unsigned)units), 256, 0, s>>>(p);
-          kern<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
+          kern_sx<<<(unsigned)grid, Cfg::NT, Cfg::SMEM, s>>>(mx, mB, mC, mth, p);
           const cudaError_t e = cudaGetLastError();
           const cudaError_t ef = cudaFreeAsync(buf, s);
           record_launch(M3_TEST_KERNEL_CHUNKED_SPLIT, grid, (long long)bytes);
