@@ -177,10 +177,14 @@ struct ChunkCfg {
   // so it and the per-chunk scalars rotate through XB slots: three when they
   // fit) and R (MN-major); S' lives in TMEM
   static constexpr int RT_BYTES = N * P * 2;
-  static constexpr int smem_for(int xb) { return 2 * STAGE + xb * XT_BYTES + RT_BYTES + 1024; }
+  static constexpr int smem_for(int ns, int xb) { return ns * STAGE + xb * XT_BYTES + RT_BYTES + 1024; }
   static constexpr int STATIC_EST = 3 * 6 * Q * 4 + (NPRO / K2) * K2 * 4 + 2048;  // scalars, scan, misc
-  static constexpr int XB = smem_for(3) + STATIC_EST <= 232448 ? 3 : 2;
-  static constexpr int OFF_XB = 2 * STAGE;
+  static constexpr int XB = smem_for(2, 3) + STATIC_EST <= 232448 ? 3 : 2;
+  // stages of the full pass: three at rank 1 when they fit (N = 64), else
+  // two (at rank 4 a third stage measured slower: the prologue runs further
+  // ahead of the state warps, the tighter role there)
+  static constexpr int NSF = R == 1 && smem_for(3, XB) + STATIC_EST <= 232448 ? 3 : 2;
+  static constexpr int OFF_XB = NSF * STAGE;
   static constexpr int OFF_RT = OFF_XB + XB * XT_BYTES;
   static constexpr int SMEM = OFF_RT + RT_BYTES + 1024;  // + alignment slack
   // state-only pass: a stage without its C tiles (from the B tiles on)
@@ -434,10 +438,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
   constexpr bool xc_pro = XC && !SO && R == 1;
 
   uint8_t* Rt = sm + Cfg::OFF_RT;
-  // Stages: two in the full pass; three in the state-only pass, whose stages
-  // hold no C tiles (stage s there starts OFF_B bytes before its B tiles,
-  // which follow the previous stage's last tile; its C offsets are unused).
-  constexpr int NS = SO ? 3 : 2;
+  // Stages: in the full pass three at rank 1 with N = 64, else two; three
+  // in the state-only pass, whose stages hold no C tiles (stage s there
+  // starts OFF_B bytes before its B tiles, which follow the previous
+  // stage's last tile; its C offsets are unused).
+  constexpr int NS = SO ? 3 : Cfg::NSF;
   static_assert(!SO || 3 * Cfg::SO_STRIDE <= Cfg::SMEM - 1024, "three state-only stages");
   auto stage = [&](int s) { return SO ? sm + s * Cfg::SO_STRIDE - Cfg::OFF_B : sm + s * Cfg::STAGE; };
   auto xbuf = [&](int x) { return sm + Cfg::OFF_XB + x * Cfg::XT_BYTES; };
@@ -1071,9 +1076,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     // theta, or its own area) parts: after the prologue of chunk c (its
     // weights, and its last read of theta)
     auto xconv = [&](int c) -> bool {
-      const int s = c & 1, xs = c % XB;
+      const int s = c % NS, xs = c % XB;
       uint8_t* stg = stage(s);
-      bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag);
+      bool got = wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c / NS) & 1), abort_flag);
       if (!SO && got && c >= XB) got = wait_xfree(c - XB);  // (SO: no X slot)
       if (!group_and(2, NSTA, got)) return false;
       {
@@ -1255,11 +1260,11 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     if (lane == 0 && warp == Cfg::W_MMA && !SO) {  // (the state-only pass has no intra-chunk products)
       // intra-chunk products, MMA 1 one chunk ahead of MMA 2
       auto mma1 = [&](int c) -> bool {
-        const int s = c & 1;
-        uint8_t* stg = stage(s);
+        const int s = c & 1, sg = c % NS;  // S buffer, stage
+        uint8_t* stg = stage(sg);
         const uint32_t Ct = saddr(stg + Cfg::OFF_C), Bt = saddr(stg + Cfg::OFF_B);
         const uint32_t Clo = saddr(stg + Cfg::OFF_CLO), Blo = saddr(stg + Cfg::OFF_BLO);
-        if (!wait_or_abort(saddr(&bar_opready[s]), (uint32_t)((c >> 1) & 1), abort_flag)) return false;
+        if (!wait_or_abort(saddr(&bar_opready[sg]), (uint32_t)((c / NS) & 1), abort_flag)) return false;
         // S[s] last held the S' of chunk c - 2: MMA 2 of that chunk, issued
         // before this by this thread, read it (tcgen05 MMAs of one thread run
         // in issue order), after S -> S' of chunk c - 2 was done
@@ -1276,7 +1281,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           }
         }
         mma_commit(saddr(&bar_sfull[s]));
-        mma_commit(saddr(&bar_free[s]));
+        mma_commit(saddr(&bar_free[sg]));
         return true;
       };
       // intra-chunk products, MMA 1 one chunk ahead of MMA 2
