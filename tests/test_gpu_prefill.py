@@ -249,8 +249,9 @@ def test_full_size_every_output(name):
 
 
 @pytest.mark.parametrize("shape", [dict(dstate=128, rank=1, chunk=64), dict(dstate=64, rank=4, chunk=16),
-                                   dict(dstate=128, rank=1, chunk=64, real=True, euler=True)],
-                         ids=["siso", "mimo4", "mamba2"])
+                                   dict(dstate=128, rank=1, chunk=64, real=True, euler=True),
+                                   dict(dstate=64, rank=1, chunk=64)],
+                         ids=["siso", "mimo4", "mamba2", "siso_n64"])
 def test_balanced_schedule_with_state(shape):
     """More units than SMs (5 x 32 heads, L 600 with a ragged last chunk):
     the chunked kernel cuts units between CTAs and hands state and carry
