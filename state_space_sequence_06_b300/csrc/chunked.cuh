@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(saddr(&bar_sfull[s]), 1);
       mbar_init(saddr(&bar_yfull[s]), 2);  // MMA 2 and MMA 3 completions
-      mbar_init(saddr(&bar_spready[s]), 1);
+      mbar_init(saddr(&bar_spready[s]), NPRO);  // every prologue thread (one arrival per warp of 32)
     }
     for (int x = 0; x < XB; ++x) {
       // MMA 2 completion and the output epilogue (SO: the state warps, once
@@ -760,8 +760,9 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
     auto scores = [&](int c) -> bool {
       const int s = c & 1, xs = c % XB;
       const float lam_end = sLamEnd[xs];
-      const bool got = wait_or_abort(saddr(&bar_sfull[s]), (uint32_t)((c >> 1) & 1), abort_flag);
-      // (the vote on `got` is taken at the closing barrier, as in the prologue)
+      // (a wait that gave up sets the CTA's abort flag: the next prologue's
+      // vote sees it, and this step computes on whatever TMEM holds)
+      wait_or_abort(saddr(&bar_sfull[s]), (uint32_t)((c >> 1) & 1), abort_flag);
       tc_fence_after();
       // warp w covers accumulator rows 16(w%4) .. +15 (TMEM lane quarter w%4)
       // and one slice of CPH columns; with the 16x256b shape thread `lane`
@@ -824,10 +825,10 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
         }
         tmem_st16x256b_x2(ta, wv);
       }
+      // each warp signals its own columns to MMA 2: no barrier of the group
       tmem_st_wait();
       tc_fence_before();
-      if (!group_and(1, NPRO, got)) return false;
-      if (pt == 0) mbar_arrive(saddr(&bar_spready[s]));
+      mbar_arrive_warp(saddr(&bar_spready[s]));
       return true;
     };
     // the prologue runs one chunk ahead of S -> S', which waits for MMA 1
