@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       // MMA 2 completion and the output epilogue (SO: the state warps, once
       // the slot's scalars are no longer read)
       mbar_init(saddr(&bar_xfree[x]), SO ? 1 : 2);
-      mbar_init(saddr(&bar_xready[x]), 1);  // the state warps' conversion of X (not in SO)
+      mbar_init(saddr(&bar_xready[x]), 1);  // X converted (state or prologue warps; not in SO)
       mbar_init(saddr(&bar_phend[x]), K2);  // the phase after the slot's chunk, one arrival per pair
     }
     mbar_init(saddr(&bar_stready), 1);
@@ -1218,8 +1218,8 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
       if (tt == 0) mbar_arrive(saddr(&bar_xfree[xs]));
       return true;
     };
-    // order, chunk n after chunk: X of chunk n as soon as its prologue is
-    // done, the output of chunk n - 1 (after its MMAs 2 and 3), then the
+    // order, chunk n after chunk: X of chunk n (unless XC) after its prologue,
+    // the output of chunk n - 1 (after its MMAs 2 and 3), then the
     // state step of chunk n (its R is needed by the next MMA 3 long before
     // the stage is released).  A segment's initial state is loaded before
     // its first chunk and its final state written after its last, outside
@@ -1339,7 +1339,7 @@ __global__ void __launch_bounds__(ChunkCfg<N, R, Q, RE>::NT, 1)
           mma_commit(saddr(&bar_rfree));
           mma_commit(saddr(&bar_yfull[s]));
         }
-        // W X converted (the state warps; SO: the prologue, with the
+        // W X converted (state warps; XC and SO: the prologue, with the
         // operands); the buffer's previous chunk-local state folded into the
         // state (S_{c-1}; SO: S_{c-2})
         if (!SO && !wait_or_abort(saddr(&bar_xready[c % XB]), (uint32_t)((c / XB) & 1), abort_flag)) break;
