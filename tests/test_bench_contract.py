@@ -50,3 +50,60 @@ def test_reference_arm_prints_one_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert set(line["e2e"]) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
     assert set(line["cpu_baseline"]) >= {"value", "cores", "kind", "sample"}
+
+
+class _FakeNvml:
+    """Stands in for the NVML library (reading only): a scripted SM clock
+    and throttle-reason word per query."""
+
+    def __init__(self, script):
+        self.script, self.calls = list(script), 0
+
+    def _next(self):
+        i = min(self.calls, len(self.script) - 1)
+        return self.script[i]
+
+    def nvmlDeviceGetClockInfo(self, h, kind, ref):
+        ref._obj.value = self._next()[0]
+        return 0
+
+    def reasons(self, h, ref):
+        ref._obj.value = self._next()[1]
+        self.calls += 1
+        return 0
+
+
+def test_clock_sampler_keeps_only_the_timed_region():
+    """The sampler drops what it saw before restart() (the warm-up), takes a
+    sample at the region's start, decodes the throttle-reason bits and stops
+    its thread on exit; a box without NVML reports the error, no samples."""
+    import ctypes
+    import time
+
+    fake = _FakeNvml([(1500, 0x8)] * 3 + [(2032, 0x4)])  # warm-up: hw_slowdown; region: sw_power_cap
+    clk = bench.ClockSampler(0, period_s=0.001)
+
+    def fake_open():
+        clk.lib, clk.h, clk.ct, clk.max_mhz = fake, ctypes.c_void_p(), ctypes, 2032
+        clk.get_reasons = fake.reasons
+
+    clk._open = fake_open
+    with clk:
+        while fake.calls < 4:  # the warm-up's three samples are all in (the thread samples in turn)
+            time.sleep(0.001)
+        clk.restart()
+        time.sleep(0.01)
+    s = clk.summary()
+    assert not clk.th.is_alive()
+    assert s["sm_mhz"] == 2032 and s["sm_max_mhz"] == 2032 and s["samples"] >= 1
+    assert s["reasons"] == ["sw_power_cap"], s
+
+    bad = bench.ClockSampler(0)
+
+    def no_nvml():
+        raise OSError("libnvidia-ml.so.1: cannot open shared object file")
+
+    bad._open = no_nvml
+    with bad:
+        bad.restart()
+    assert bad.summary()["sm_mhz"] is None and "no samples" not in bad.summary()["reasons"][0]
